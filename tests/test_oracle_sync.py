@@ -1,0 +1,167 @@
+"""Pins the oracle's on-policy weight-sync model: round trip is bit-identical,
+corruption is detected, the layout is as specified, and the naive off-policy
+path (dequantize -> bf16 -> per-tensor re-quantize) does NOT reproduce the
+trainer's FP8 weights while the sync path does."""
+import numpy as np
+import pytest
+
+from block_scaled_fp8_e4m3_gb300 import synth
+from conftest import read_golden
+
+
+def _specs(orc, seed=0):
+    W = synth.random_bf16((256, 384), seed=seed + 1, std=0.02)
+    cw, sw = orc.quant_block_128x128(synth.bf16_bits(W))
+    X = synth.random_bf16((130, 256), seed=seed + 2, outliers=True)
+    cx, sx = orc.quant_group_1x128(synth.bf16_bits(X))
+    M = synth.random_bf16((100, 96), seed=seed + 3)
+    cm, sm = orc.quant_mx_1x32(synth.bf16_bits(M))
+    N = synth.random_bf16((3, 70), seed=seed + 4)
+    return [
+        dict(tag=0x1111, kind=orc.KIND_FP8, recipe=orc.RECIPE_BLOCKWISE, rows=256, cols=384,
+             layout=orc.LAYOUT_BLOCK_128x128, data=cw, scales=sw),
+        dict(tag=0x2222, kind=orc.KIND_FP8, recipe=orc.RECIPE_BLOCKWISE, rows=130, cols=256,
+             layout=orc.LAYOUT_GROUP_1x128, data=cx, scales=sx),
+        dict(tag=0x3333, kind=orc.KIND_FP8, recipe=orc.RECIPE_MX, rows=100, cols=96,
+             layout=orc.LAYOUT_MX_1x32, data=cm, scales=sm),
+        dict(tag=0x4444, kind=orc.KIND_BF16, recipe=orc.RECIPE_NONE, rows=3, cols=70,
+             layout=orc.LAYOUT_NONE, data=synth.bf16_bits(N), scales=None),
+    ]
+
+
+def _empty_like(specs):
+    out = []
+    for s in specs:
+        d = dict(s)
+        d["data"] = np.zeros_like(s["data"])
+        d["scales"] = None if s["scales"] is None else np.zeros_like(s["scales"])
+        out.append(d)
+    return out
+
+
+def _rd(p, off, n):
+    return int.from_bytes(bytes(p[off:off + n]), "little")
+
+
+def test_round_trip_bit_identical(orc):
+    specs = _specs(orc)
+    payload = orc.sync_pack(specs)
+    dst = _empty_like(specs)
+    assert orc.sync_install(payload, dst) == 0
+    for s, d in zip(specs, dst):
+        assert np.array_equal(s["data"], d["data"])
+        if s["scales"] is not None:
+            assert s["scales"].tobytes() == d["scales"].tobytes()
+
+
+def test_layout(orc):
+    specs = _specs(orc)
+    p = orc.sync_pack(specs)
+    assert bytes(p[:8]) == b"FP8SYNC1"
+    assert _rd(p, 8, 4) == 1 and _rd(p, 12, 4) == len(specs)
+    total = _rd(p, 16, 8)
+    assert total == p.size and total % 256 == 0
+    assert _rd(p, 24, 8) == 768                       # roundup(64 + 4*128, 256)
+    prev_end = 768
+    for i, s in enumerate(specs):
+        t = 64 + 128 * i
+        doff, dbytes = _rd(p, t + 40, 8), _rd(p, t + 48, 8)
+        soff, sbytes = _rd(p, t + 56, 8), _rd(p, t + 64, 8)
+        assert doff % 256 == 0 and doff >= prev_end
+        assert dbytes == s["data"].nbytes
+        assert bytes(p[doff:doff + dbytes]) == s["data"].tobytes()
+        prev_end = doff + dbytes
+        if s["scales"] is not None:
+            assert soff % 256 == 0 and soff >= prev_end and sbytes == s["scales"].nbytes
+            assert bytes(p[soff:soff + sbytes]) == s["scales"].tobytes()
+            prev_end = soff + sbytes
+        else:
+            assert soff == 0 and sbytes == 0
+        assert not np.any(p[t + 72:t + 128])
+    # padding is zero
+    assert _rd(p, 40, 24) == 0
+
+
+def test_splitmix64_published_outputs(orc):
+    """The finaliser used by the checksum reproduces the published first
+    outputs of the splitmix64 generator started from state 0."""
+    rows = read_golden("splitmix64.txt")
+    gamma = 0x9E3779B97F4A7C15
+    for i, row in enumerate(rows):
+        assert orc.splitmix64((gamma * i) & (2 ** 64 - 1)) == int(row[1], 16)
+
+
+def test_checksum_detects_any_single_word_change(orc):
+    specs = _specs(orc)
+    p = orc.sync_pack(specs)
+    base = orc.sync_checksum(p)
+    assert base == _rd(p, 32, 8)
+    rng = np.random.default_rng(5)
+    for off in list(range(64, p.size, 8))[::7]:
+        q = p.copy()
+        q[off + rng.integers(0, 8)] ^= 1 << int(rng.integers(0, 8))
+        assert orc.sync_checksum(q) != base
+    # header words (bytes 0..63) are not covered by the sum
+    q = p.copy()
+    q[40] = 1
+    assert orc.sync_checksum(q) == base
+
+
+@pytest.mark.parametrize("where", ["data", "table", "magic", "count", "shape", "tag"])
+def test_install_rejects_corruption(orc, where):
+    specs = _specs(orc)
+    p = orc.sync_pack(specs)
+    dst = _empty_like(specs)
+    expect = 2
+    if where == "data":
+        p[_rd(p, 64 + 40, 8) + 5] ^= 0x10
+    elif where == "table":
+        p[64 + 72] = 1                                  # reserved byte, covered by checksum
+    elif where == "magic":
+        p[0] ^= 1
+        expect = 1
+    elif where == "count":
+        dst = dst[:3]
+        expect = 1
+    elif where == "shape":
+        dst[0]["rows"] = 128
+        dst[0]["data"] = dst[0]["data"][:128].copy()
+        dst[0]["scales"] = dst[0]["scales"][:1].copy()
+        expect = 1
+    elif where == "tag":
+        dst[1]["tag"] = 0x9999
+        expect = 1
+    assert orc.sync_install(p, dst) == expect
+    for d in dst:
+        assert not np.any(d["data"])                    # nothing written
+
+
+def test_naive_off_policy_differs_sync_does_not(orc):
+    """The per-tensor re-quantization of the dequantized BF16 weights does not
+    reproduce the trainer's FP8 representation; the sync payload does."""
+    W = synth.tiny().tensors["W"]
+    w = W.double().numpy()
+    cw, sw = orc.quant_block_128x128(synth.bf16_bits(W))
+    naive_codes, s_naive = orc.naive_requant_per_tensor(cw, sw)
+    # the block holding the tensor maximum round-trips exactly (its max code
+    # is 448 * s and the product is bf16-representable), so the per-tensor
+    # scale equals the largest block scale; every other block gets a scale
+    # that is not its own, and its codes change
+    assert s_naive == sw.max()
+    trainer = orc.dequant_block(cw, sw)
+    rollout = orc.e4m3_decode(naive_codes) * s_naive
+    nb, kb = np.unravel_index(int(np.argmax(sw)), sw.shape)
+    same = np.zeros_like(trainer, dtype=bool)
+    same[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128] = True
+    assert np.array_equal(trainer[same], rollout[same])
+    assert np.count_nonzero(trainer[~same] != rollout[~same]) > 0.5 * np.count_nonzero(~same)
+    # the synthetic analogue of the mismatch figure (reported, not pinned)
+    rel = np.abs(rollout - trainer).mean() / np.abs(trainer).mean()
+    q_err = np.abs(trainer - w).mean() / np.abs(w).mean()
+    assert rel > 0 and q_err > 0
+    # sync path: identical
+    spec = [dict(tag=1, kind=orc.KIND_FP8, recipe=orc.RECIPE_BLOCKWISE, rows=512, cols=512,
+                 layout=orc.LAYOUT_BLOCK_128x128, data=cw, scales=sw)]
+    dst = _empty_like(spec)
+    assert orc.sync_install(orc.sync_pack(spec), dst) == 0
+    assert np.array_equal(orc.dequant_block(dst[0]["data"], dst[0]["scales"]), trainer)
