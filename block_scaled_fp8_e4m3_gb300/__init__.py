@@ -1,1 +1,313 @@
-"""Block-scaled FP8 (E4M3) quantization, GEMM and weight sync for GB300."""
+"""Block-scaled FP8 (E4M3) quantization, GEMM and on-policy weight sync for
+GB300 (sm_103a).
+
+A thin ctypes binding over ``libfp8bs.so`` (C ABI in ``include/fp8bs.h``).
+PyTorch provides device memory and streams; every step of the computation
+runs in the library's CUDA kernels.  There is no CPU path: every call raises
+if the compiled library or a CUDA device is missing.
+
+Shapes follow ``torch.nn.Linear``: X [M, K], W [N, K], Y = X W^T.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+__all__ = [
+    "FP8Error", "QTensor", "SyncEntry", "library", "quantize_group", "quantize_block", "quantize_mx",
+    "permute_rows_mx", "gemm", "grouped_gemm", "sync_payload_size", "sync_pack", "sync_install",
+    "status_poll", "mx_scale_bytes", "mx_grouped_scale_bytes",
+    "RECIPE_BLOCKWISE", "RECIPE_MX", "LAYOUT_GROUP_1x128", "LAYOUT_BLOCK_128x128", "LAYOUT_MX_1x32",
+    "LAYOUT_MX_1x32_GROUPED",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfp8bs.so")
+
+RECIPE_BLOCKWISE, RECIPE_MX = 1, 2
+LAYOUT_GROUP_1x128, LAYOUT_BLOCK_128x128, LAYOUT_MX_1x32, LAYOUT_MX_1x32_GROUPED = 1, 2, 3, 4
+AXIS_K, AXIS_M = 0, 1
+OP = {"fwd": 0, "dgrad": 1, "wgrad": 2}
+OUT_BF16, OUT_F32 = 0, 1
+SYNC_FP8, SYNC_BF16 = 1, 2
+
+_STATUS = {0: "FP8_OK", 1: "FP8_ERR_INVALID_ARG", 2: "FP8_ERR_ALIGNMENT", 3: "FP8_ERR_UNSUPPORTED",
+           4: "FP8_ERR_BAD_PAYLOAD", 5: "FP8_ERR_CHECKSUM", 6: "FP8_ERR_TIMEOUT", 7: "FP8_ERR_CUDA",
+           8: "FP8_ERR_CAPACITY"}
+
+
+class FP8Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class _Tensor(C.Structure):
+    _fields_ = [("codes", C.c_void_p), ("scales", C.c_void_p), ("rows", C.c_int64), ("cols", C.c_int64),
+                ("recipe", C.c_int32), ("layout", C.c_int32)]
+
+
+class _SyncEntry(C.Structure):
+    _fields_ = [("tag", C.c_uint64), ("kind", C.c_int32), ("reserved", C.c_int32), ("t", _Tensor)]
+
+
+_lib = None
+
+
+def library() -> C.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise FP8Error(7, f"{LIB_PATH} is missing: run __graft_entry__.build() first")
+    lib = C.CDLL(LIB_PATH)
+    P, I64, I32, S = C.c_void_p, C.c_int64, C.c_int32, C.c_void_p
+    TP = C.POINTER(_Tensor)
+    EP = C.POINTER(_SyncEntry)
+    sigs = {
+        "fp8_quantize_group": [P, I64, I64, I64, I32, TP, S],
+        "fp8_quantize_block": [P, I64, I64, I64, TP, TP, S],
+        "fp8_quantize_mx": [P, I64, I64, I64, TP, S],
+        "fp8_permute_rows_mx": [TP, P, P, I32, TP, S],
+        "fp8_gemm_blockscaled": [TP, TP, P, I64, I32, I32, TP, S],
+        "fp8_grouped_gemm": [TP, TP, P, I32, I64, P, I64, S],
+        "fp8_sync_payload_size": [EP, I32, C.POINTER(C.c_uint64)],
+        "fp8_sync_pack": [EP, I32, P, C.c_uint64, C.POINTER(C.c_uint64), S],
+        "fp8_sync_install": [P, C.c_uint64, EP, I32, S],
+        "fp8_status_poll": [S],
+    }
+    for name, args in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = C.c_int
+    lib.fp8_last_error.restype = C.c_char_p
+    lib.fp8_last_error.argtypes = []
+    lib.fp8_abi_version.restype = C.c_int32
+    lib.fp8_mx_scale_bytes.restype = C.c_int64
+    lib.fp8_mx_scale_bytes.argtypes = [I64, I64]
+    lib.fp8_mx_grouped_scale_bytes.restype = C.c_int64
+    lib.fp8_mx_grouped_scale_bytes.argtypes = [I64, I64, I32]
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise FP8Error(status, library().fp8_last_error().decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dev(t: torch.Tensor) -> torch.device:
+    if not t.is_cuda:
+        raise FP8Error(1, "inputs must be CUDA tensors (there is no CPU path)")
+    return t.device
+
+
+@dataclass
+class QTensor:
+    """A quantized matrix: E4M3 codes [rows, cols] (uint8) and its scales."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    rows: int
+    cols: int
+    recipe: int
+    layout: int
+
+    def c(self) -> _Tensor:
+        return _Tensor(self.codes.data_ptr(), self.scales.data_ptr(), self.rows, self.cols, self.recipe,
+                       self.layout)
+
+
+def mx_scale_bytes(rows: int, cols: int) -> int:
+    return int(library().fp8_mx_scale_bytes(rows, cols))
+
+
+def mx_grouped_scale_bytes(total_rows: int, cols: int, groups: int) -> int:
+    return int(library().fp8_mx_grouped_scale_bytes(total_rows, cols, groups))
+
+
+def _bf16_2d(x: torch.Tensor) -> torch.Tensor:
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise FP8Error(1, "expected a 2-D bf16 tensor with unit column stride")
+    return x
+
+
+# ---------------------------------------------------------------- quantizers
+def quantize_group(x: torch.Tensor, axis: str = "K", stream=None) -> QTensor:
+    """1x128 groups along K (axis='K') or 128x1 groups along M written
+    transposed (axis='M', the WGrad operand layout)."""
+    x = _bf16_2d(x)
+    M, K = x.shape
+    dev = _dev(x)
+    if axis == "K":
+        q = QTensor(torch.empty((M, K), dtype=torch.uint8, device=dev),
+                    torch.empty((K // 128, M), dtype=torch.float32, device=dev), M, K, RECIPE_BLOCKWISE,
+                    LAYOUT_GROUP_1x128)
+        ax = AXIS_K
+    elif axis == "M":
+        q = QTensor(torch.empty((K, M), dtype=torch.uint8, device=dev),
+                    torch.empty((M // 128, K), dtype=torch.float32, device=dev), K, M, RECIPE_BLOCKWISE,
+                    LAYOUT_GROUP_1x128)
+        ax = AXIS_M
+    else:
+        raise FP8Error(1, f"axis must be 'K' or 'M', got {axis!r}")
+    t = q.c()
+    _check(library().fp8_quantize_group(x.data_ptr(), M, K, x.stride(0), ax, C.byref(t), _stream(stream)))
+    return q
+
+
+def quantize_block(w: torch.Tensor, transposed: bool = False, stream=None):
+    """128x128 blocks; with transposed=True also returns the transposed copy
+    (codes [K, N], scales [K/128, N/128]) used as the DGrad B operand."""
+    w = _bf16_2d(w)
+    N, K = w.shape
+    dev = _dev(w)
+    q = QTensor(torch.empty((N, K), dtype=torch.uint8, device=dev),
+                torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev), N, K, RECIPE_BLOCKWISE,
+                LAYOUT_BLOCK_128x128)
+    qt = None
+    if transposed:
+        qt = QTensor(torch.empty((K, N), dtype=torch.uint8, device=dev),
+                     torch.empty((K // 128, N // 128), dtype=torch.float32, device=dev), K, N,
+                     RECIPE_BLOCKWISE, LAYOUT_BLOCK_128x128)
+    t = q.c()
+    tt = qt.c() if qt is not None else None
+    _check(library().fp8_quantize_block(w.data_ptr(), N, K, w.stride(0), C.byref(t),
+                                        C.byref(tt) if tt is not None else None, _stream(stream)))
+    return (q, qt) if transposed else q
+
+
+def quantize_mx(x: torch.Tensor, stream=None) -> QTensor:
+    """MXFP8: 1x32 blocks, E8M0 scales in the tensor-core atom layout."""
+    x = _bf16_2d(x)
+    R, K = x.shape
+    dev = _dev(x)
+    q = QTensor(torch.empty((R, K), dtype=torch.uint8, device=dev),
+                torch.empty((mx_scale_bytes(R, K),), dtype=torch.uint8, device=dev), R, K, RECIPE_MX,
+                LAYOUT_MX_1x32)
+    t = q.c()
+    _check(library().fp8_quantize_mx(x.data_ptr(), R, K, x.stride(0), C.byref(t), _stream(stream)))
+    return q
+
+
+def permute_rows_mx(q: QTensor, gather: torch.Tensor, offsets: torch.Tensor, stream=None) -> QTensor:
+    """Gathers MX rows into expert-contiguous groups (dst row i = src row
+    gather[i]); offsets int32 [G+1] on the device."""
+    if gather.dtype != torch.int32 or offsets.dtype != torch.int32:
+        raise FP8Error(1, "gather and offsets must be int32")
+    total = gather.numel()
+    G = offsets.numel() - 1
+    dev = _dev(q.codes)
+    out = QTensor(torch.empty((total, q.cols), dtype=torch.uint8, device=dev),
+                  torch.empty((mx_grouped_scale_bytes(total, q.cols, G),), dtype=torch.uint8, device=dev),
+                  total, q.cols, RECIPE_MX, LAYOUT_MX_1x32_GROUPED)
+    src, dst = q.c(), out.c()
+    _check(library().fp8_permute_rows_mx(C.byref(src), gather.data_ptr(), offsets.data_ptr(), G, C.byref(dst),
+                                         _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------- GEMMs
+def gemm(A: QTensor, B: QTensor, op: str = "fwd", out_dtype=torch.bfloat16, quantize_output: bool = False,
+         out: Optional[torch.Tensor] = None, stream=None):
+    """D = A B^T with fp32 accumulation.  Returns D, or (D, QTensor of D)
+    when quantize_output (1x128 for blockwise, 1x32 for MXFP8)."""
+    M, N = A.rows, B.rows
+    dev = _dev(A.codes)
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=dev)
+    dq = None
+    if quantize_output:
+        if A.recipe == RECIPE_BLOCKWISE:
+            dq = QTensor(torch.empty((M, N), dtype=torch.uint8, device=dev),
+                         torch.empty((N // 128, M), dtype=torch.float32, device=dev), M, N, RECIPE_BLOCKWISE,
+                         LAYOUT_GROUP_1x128)
+        else:
+            dq = QTensor(torch.empty((M, N), dtype=torch.uint8, device=dev),
+                         torch.empty((mx_scale_bytes(M, N),), dtype=torch.uint8, device=dev), M, N, RECIPE_MX,
+                         LAYOUT_MX_1x32)
+    a, b = A.c(), B.c()
+    dqc = dq.c() if dq is not None else None
+    dt = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(library().fp8_gemm_blockscaled(C.byref(a), C.byref(b), out.data_ptr(), out.stride(0), dt, OP[op],
+                                          C.byref(dqc) if dqc is not None else None, _stream(stream)))
+    return (out, dq) if quantize_output else out
+
+
+def grouped_gemm(A: QTensor, B_stack: QTensor, offsets: torch.Tensor, N: int, out: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    """Per-expert D[off_g:off_g+1] = A_g W_g^T (MXFP8)."""
+    G = offsets.numel() - 1
+    if out is None:
+        out = torch.empty((A.rows, N), dtype=torch.bfloat16, device=_dev(A.codes))
+    a, b = A.c(), B_stack.c()
+    _check(library().fp8_grouped_gemm(C.byref(a), C.byref(b), offsets.data_ptr(), G, N, out.data_ptr(),
+                                      out.stride(0), _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------- weight sync
+@dataclass
+class SyncEntry:
+    """One tensor of a weight-sync payload: a QTensor, or a bf16 tensor kept
+    in high precision (norms, embeddings)."""
+    tag: int
+    tensor: object  # QTensor or bf16 torch.Tensor
+
+    def c(self) -> _SyncEntry:
+        if isinstance(self.tensor, QTensor):
+            return _SyncEntry(self.tag, SYNC_FP8, 0, self.tensor.c())
+        t = self.tensor
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_contiguous():
+            raise FP8Error(1, "bf16 sync entries must be contiguous 2-D bf16 tensors")
+        return _SyncEntry(self.tag, SYNC_BF16, 0, _Tensor(t.data_ptr(), None, t.shape[0], t.shape[1], 0, 0))
+
+
+def _entries(entries: Sequence[SyncEntry]):
+    arr = (_SyncEntry * max(1, len(entries)))()
+    for i, e in enumerate(entries):
+        arr[i] = e.c()
+    return arr
+
+
+def sync_payload_size(entries: Sequence[SyncEntry]) -> int:
+    n = C.c_uint64(0)
+    _check(library().fp8_sync_payload_size(_entries(entries), len(entries), C.byref(n)))
+    return int(n.value)
+
+
+def sync_pack(entries: Sequence[SyncEntry], payload: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Packs the trainer's FP8 codes + scales (and bf16 tensors) into one
+    device payload."""
+    size = sync_payload_size(entries)
+    if payload is None:
+        dev = entries[0].tensor.codes.device if isinstance(entries[0].tensor, QTensor) else entries[0].tensor.device
+        payload = torch.empty((size,), dtype=torch.uint8, device=dev)
+    used = C.c_uint64(0)
+    _check(library().fp8_sync_pack(_entries(entries), len(entries), payload.data_ptr(), payload.numel(),
+                                   C.byref(used), _stream(stream)))
+    return payload[: used.value]
+
+
+def sync_install(payload: torch.Tensor, dst: Sequence[SyncEntry], stream=None, check: bool = True):
+    """Installs a payload into the rollout-side tensors (no quantizer runs).
+    With check=True the device-side checksum verdict is read back and a
+    mismatch raises FP8Error(FP8_ERR_CHECKSUM)."""
+    _check(library().fp8_sync_install(payload.data_ptr(), payload.numel(), _entries(dst), len(dst),
+                                      _stream(stream)))
+    if check:
+        status_poll(stream)
+
+
+def status_poll(stream=None):
+    _check(library().fp8_status_poll(_stream(stream)))

@@ -1,0 +1,726 @@
+// gemm.cu -- block-scaled FP8 GEMMs on the 5th-generation tensor cores.
+//
+// Both kernels compute D = A B^T with A [M][K], B [N][K] E4M3 codes (K-major)
+// and are persistent, warp-specialised, one CTA per SM, 10 warps:
+//   warp 0      TMA producer: A and B tiles (+ the MX scale atoms) per
+//               128-wide K block into a multi-stage shared-memory ring
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma (M=128, K=32,
+//               four per K block) and tcgen05.commit
+//   warps 2-9   epilogue: tcgen05.ld of the fp32 accumulator; warp w owns TMEM
+//               lanes 32*(w%4).. and half of the tile's columns, so each lane
+//               quarter is served by two warps.
+// Ten warps put three warps on two of the four SM sub-partitions, whose
+// 16K-register files then allow at most 168 registers per thread; the tile
+// shapes below are chosen so that the epilogue fits without spilling.
+//
+// Blockwise recipe (fp32 scales; "Jet-RL: Enabling On-Policy FP8 ...",
+// "Kwantisatieschema"): the fp32 scales cannot be applied inside the MMA, so
+// each K block is accumulated into a fresh TMEM buffer P (kind::f8f6f4) and
+// the epilogue warps promote it into register accumulators:
+//   acc[m][n] += P[m][n] * sa[kb][m] * sb(n, kb)
+// with sb per 128x128 weight block (forward, DGrad) or per row of B (WGrad,
+// whose operands come from 128x1 groups).  Tile 128x128 (64 accumulators per
+// epilogue thread); P double-buffered (2 x 128 TMEM columns) so the tensor
+// core fills one while the other is promoted; 6-stage ring.
+//
+// MXFP8 recipe ("Anyscale、SkyRL で FP8 ...", "Deep dive: FP8 quantization
+// with FP32 and power-of-two block scales": Blackwell tensor cores apply
+// power-of-two block scales themselves): kind::mxf8f6f4.block_scale with the
+// E8M0 scale atoms copied shared -> TMEM by tcgen05.cp; the accumulator stays
+// in TMEM for the whole K loop.  Tile 128x256, 4-stage ring.  The grouped
+// (MoE) variant walks a tile list over (expert, 128-row tile, 256-col tile).
+//
+// Every wait is bounded (see mbar_wait_bounded); on expiry the kernel records
+// FP8_ERR_TIMEOUT, lets in-flight copies and MMAs land, frees TMEM, and exits.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8bs {
+
+namespace {
+
+constexpr int BM = 128, BK = 128;
+constexpr int kThreads = 320;
+constexpr int kEpiWarp0 = 2;
+constexpr int kEpiThreads = 256;
+constexpr int kMaxStages = 6;
+constexpr int kMaxGroups = 1024;
+
+// blockwise kernel
+constexpr int kBwBN = 128;
+constexpr int kBwStages = 6;
+constexpr uint32_t kBwStageBytes = (BM + kBwBN) * BK;  // 32 KB
+constexpr uint32_t kBwTmemCols = 256;                   // two P buffers of 128 columns
+constexpr uint32_t kIdescBlockwise = idesc_f8f6f4(BM, kBwBN);
+
+// MX kernel
+constexpr int kMxBN = 256;
+constexpr int kMxStages = 4;
+constexpr uint32_t kMxStageBytes = (BM + kMxBN) * BK;  // 48 KB
+constexpr uint32_t kSfStageBytes = 1536;                // SFA atom + two SFB atoms
+constexpr uint32_t kMxTmemCols = 512;                   // accumulator 256 + scale factors
+
+struct Barriers {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    int num_mtiles;  // MX: total 128-row tiles over all groups
+    float amax_xch[2][128];  // blockwise fused quantization: per-half row maxima
+};
+
+constexpr size_t kSmemBlockwise = 1024 + (size_t)kBwStages * kBwStageBytes + sizeof(Barriers);
+constexpr size_t kSmemMx = 1024 + (size_t)kMxStages * (kMxStageBytes + kSfStageBytes) + sizeof(Barriers) +
+                           2 * (kMaxGroups + 1) * sizeof(int);
+
+__device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
+    const uint32_t a = smem_u32(raw);
+    return raw + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// Wait that ignores the abort flag (used to let in-flight work land).
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, StatusBlock* st) {
+    int dummy = 0;
+    mbar_wait_bounded(bar, parity, &dummy, st, 99);
+}
+
+// Empty asm that "redefines" the registers, so that no use of a TMEM load
+// result can be scheduled before the preceding tcgen05.wait::ld.
+__device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                   "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])::"memory");
+}
+
+__device__ __forceinline__ void ld_chunk(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld_32x32b_x32(taddr, r); }
+
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15])::"memory");
+}
+
+__device__ __forceinline__ void wait_chunk16(uint32_t (&r)[16]) {
+    tmem_ld_wait();
+    reg_fence16(r);
+}
+
+// acc[j] += P[j] * c for 16 columns
+__device__ __forceinline__ void promote16(float* acc, const uint32_t (&r)[16], float c) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = fmaf(__uint_as_float(r[i]), c, acc[i]);
+}
+
+// acc[j] += (P[j] * sb[j]) * sa for 16 columns with per-column scales sb
+__device__ __forceinline__ void promote16_cols(float* acc, const uint32_t (&r)[16], const float* sb, float sa) {
+    const float4* s4 = reinterpret_cast<const float4*>(sb);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 v = __ldg(s4 + i);
+        acc[4 * i + 0] = fmaf(__uint_as_float(r[4 * i + 0]) * v.x, sa, acc[4 * i + 0]);
+        acc[4 * i + 1] = fmaf(__uint_as_float(r[4 * i + 1]) * v.y, sa, acc[4 * i + 1]);
+        acc[4 * i + 2] = fmaf(__uint_as_float(r[4 * i + 2]) * v.z, sa, acc[4 * i + 2]);
+        acc[4 * i + 3] = fmaf(__uint_as_float(r[4 * i + 3]) * v.w, sa, acc[4 * i + 3]);
+    }
+}
+
+// MX 1x32 quantization of one row's 128 bf16 values: four blocks; returns
+// the four E8M0 bytes packed little-endian.
+__device__ __forceinline__ uint32_t quant_row_mx(const uint32_t (&packed)[64], uint8_t* codes) {
+    uint32_t sc = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        float a = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            a = fmaxf(a, fmaxf(fabsf(bf16_lo(packed[16 * b + j])), fabsf(bf16_hi(packed[16 * b + j]))));
+        const int e = mx_exponent(a);
+        const float mul = exp2_int(-e);
+        sc |= (uint32_t)(e + 127) << (8 * b);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t p0 = packed[16 * b + 8 * i + 2 * k], p1 = packed[16 * b + 8 * i + 2 * k + 1];
+                w[k] = e4m3x2(__fmul_rn(bf16_lo(p0), mul), __fmul_rn(bf16_hi(p0), mul)) |
+                       (e4m3x2(__fmul_rn(bf16_lo(p1), mul), __fmul_rn(bf16_hi(p1), mul)) << 16);
+            }
+            reinterpret_cast<uint4*>(codes + 32 * b)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    return sc;
+}
+
+// ===========================================================================
+// Blockwise (fp32-scale) GEMM with promotion
+// ===========================================================================
+struct BwParams {
+    const float* sa;
+    const float* sb;
+    int sb_per_row;
+    int M, N, K;
+    void* D;
+    long long ldd;
+    int d_f32;
+    uint8_t* q_codes;
+    float* q_scales;
+    StatusBlock* st;
+    int tiles_m, tiles_n;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_blockwise(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const BwParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = aligned_smem(smem_raw);
+    Barriers* bar = reinterpret_cast<Barriers*>(smem + kBwStages * kBwStageBytes);
+    volatile int* abort = &bar->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kBwStages; ++s) {
+            mbar_init(&bar->full[s], 1);
+            mbar_init(&bar->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bar->acc_full[b], 1);
+            mbar_init(&bar->acc_empty[b], kEpiThreads);
+        }
+        mbar_init(&bar->drain, 1);
+        bar->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) tmem_alloc(&bar->tmem_base, kBwTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar->tmem_base;
+    const int KB = p.K / BK;
+    const int num_tiles = p.tiles_m * p.tiles_n;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t fills[kBwStages] = {0, 0, 0, 0, 0, 0};
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                const int tm = tile / p.tiles_n, tn = tile % p.tiles_n;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait_bounded(&bar->empty[s], ph ^ 1, abort, p.st, 1)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* stage = smem + s * kBwStageBytes;
+                    mbar_arrive_expect_tx(&bar->full[s], kBwStageBytes);
+                    tma_load_2d(stage, &tmA, &bar->full[s], kb * BK, tm * BM);
+                    tma_load_2d(stage + BM * BK, &tmB, &bar->full[s], kb * BK, tn * kBwBN);
+                    ++fills[s];
+                    if (++s == kBwStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok)
+                for (int i = 0; i < kBwStages; ++i)
+                    if (fills[i]) mbar_wait_drain(&bar->full[i], (fills[i] - 1) & 1, p.st);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int s = 0, ab = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait_bounded(&bar->acc_empty[ab], aph ^ 1, abort, p.st, 2) ||
+                        !mbar_wait_bounded(&bar->full[s], ph, abort, p.st, 3)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + s * kBwStageBytes);
+                    const uint64_t adesc = sdesc_k_sw128(a_addr);
+                    const uint64_t bdesc = sdesc_k_sw128(a_addr + BM * BK);
+                    const uint32_t d = tmem + (uint32_t)(ab * kBwBN);
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        tc_mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, kIdescBlockwise, k > 0 ? 1u : 0u);
+                    tc_commit(&bar->empty[s]);
+                    tc_commit(&bar->acc_full[ab]);
+                    if (++s == kBwStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                    ab ^= 1;
+                    if (ab == 0) aph ^= 1;
+                }
+            }
+            tc_commit(&bar->drain);
+            mbar_wait_drain(&bar->drain, 0, p.st);
+        }
+    } else {
+        // epilogue: warp (q = warp%4, h) promotes rows 32q.. , columns 64h..64h+63
+        const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
+        const int rl = 32 * q + lane;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        int ab = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            const int tm = tile / p.tiles_n, tn = tile % p.tiles_n;
+            const int m = tm * BM + rl;
+            const int ncol0 = tn * kBwBN + 64 * h;
+            const bool mvalid = m < p.M;
+            float acc[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+            float sa_next = mvalid ? __ldg(p.sa + m) : 0.0f;
+            for (int kb = 0; kb < KB; ++kb) {
+                const float sa_v = sa_next;
+                if (kb + 1 < KB) sa_next = mvalid ? __ldg(p.sa + (size_t)(kb + 1) * p.M + m) : 0.0f;
+                float cs = 0.0f;
+                if (!p.sb_per_row) cs = sa_v * __ldg(p.sb + (size_t)tn * KB + kb);
+                if (!mbar_wait_bounded(&bar->acc_full[ab], aph, abort, p.st, 4)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tb = tmem + lane_base + (uint32_t)(ab * kBwBN + 64 * h);
+                // 4 chunks of 16 columns, double-buffered: chunk c+1 is in
+                // flight while chunk c is promoted
+                uint32_t r[2][16];
+                tmem_ld_32x32b_x16(tb, r[0]);
+                wait_chunk16(r[0]);
+                if (!p.sb_per_row) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        if (c < 3) tmem_ld_32x32b_x16(tb + 16 * (c + 1), r[(c + 1) & 1]);
+                        promote16(acc + 16 * c, r[c & 1], cs);
+                        if (c < 3) wait_chunk16(r[(c + 1) & 1]);
+                    }
+                } else {
+                    const float* sbs = p.sb + (size_t)kb * p.N + ncol0;  // per-column scales of B (WGrad)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        if (c < 3) tmem_ld_32x32b_x16(tb + 16 * (c + 1), r[(c + 1) & 1]);
+                        promote16_cols(acc + 16 * c, r[c & 1], sbs + 16 * c, sa_v);
+                        if (c < 3) wait_chunk16(r[(c + 1) & 1]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&bar->acc_empty[ab]);
+                ab ^= 1;
+                if (ab == 0) aph ^= 1;
+            }
+            if (!ok) break;
+            if (p.d_f32) {
+                if (mvalid) {
+                    float* d = reinterpret_cast<float*>(p.D) + (size_t)m * p.ldd + ncol0;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        reinterpret_cast<float4*>(d)[i] =
+                            make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                }
+                continue;
+            }
+            uint32_t packed[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) packed[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
+            if (mvalid) {
+                uint4* d = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.D) + (size_t)m * p.ldd + ncol0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+            }
+            if (p.q_codes != nullptr) {
+                // 1x128 group = this thread's 64 columns + the partner warp's 64:
+                // exchange the half-row maxima through shared memory
+                float a = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    a = fmaxf(a, fmaxf(fabsf(bf16_lo(packed[j])), fabsf(bf16_hi(packed[j]))));
+                bar->amax_xch[h][rl] = a;
+                asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
+                a = fmaxf(a, bar->amax_xch[h ^ 1][rl]);
+                asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
+                const float sc = group_scale(a);
+                if (mvalid) {
+                    uint8_t* codes = p.q_codes + (size_t)m * p.N + ncol0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t p0 = packed[8 * i + 2 * k], p1 = packed[8 * i + 2 * k + 1];
+                            w[k] = e4m3x2(__fdiv_rn(bf16_lo(p0), sc), __fdiv_rn(bf16_hi(p0), sc)) |
+                                   (e4m3x2(__fdiv_rn(bf16_lo(p1), sc), __fdiv_rn(bf16_hi(p1), sc)) << 16);
+                        }
+                        reinterpret_cast<uint4*>(codes)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    if (h == 0) p.q_scales[(size_t)tn * p.M + m] = sc;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kBwTmemCols);
+    }
+}
+
+// ===========================================================================
+// MXFP8 GEMM (hardware block scaling), plain or grouped
+// ===========================================================================
+struct MxParams {
+    const uint8_t* sfa;
+    const uint8_t* sfb;
+    const int32_t* m_offsets;  // nullptr: one group of M rows
+    int G;
+    int M, N, K;
+    uint16_t* D;
+    long long ldd;
+    uint8_t* q_codes;
+    uint8_t* q_scales;
+    StatusBlock* st;
+    int tiles_n;
+};
+
+struct TileCoord {
+    int g, mt_global, row0, rows, tn;  // rows = valid rows of the group in this tile
+};
+
+__device__ __forceinline__ TileCoord mx_tile(int tile, int tiles_n, const int* pfx, const int* offs, int G) {
+    TileCoord c;
+    c.mt_global = tile / tiles_n;
+    c.tn = tile % tiles_n;
+    int lo = 0, hi = G;  // largest g with pfx[g] <= mt_global
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pfx[mid] <= c.mt_global) lo = mid; else hi = mid;
+    }
+    c.g = lo;
+    const int mt = c.mt_global - pfx[lo];
+    c.row0 = offs[lo] + mt * BM;
+    const int left = offs[lo + 1] - c.row0;
+    c.rows = left < BM ? left : BM;
+    return c;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const MxParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = aligned_smem(smem_raw);
+    uint8_t* sf = smem + kMxStages * kMxStageBytes;
+    Barriers* bar = reinterpret_cast<Barriers*>(sf + kMxStages * kSfStageBytes);
+    int* offs = reinterpret_cast<int*>(bar + 1);  // [G+1] row offsets
+    int* pfx = offs + (kMaxGroups + 1);           // [G+1] prefix of 128-row tiles (= scale atom rows)
+    volatile int* abort = &bar->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.G;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kMxStages; ++s) {
+            mbar_init(&bar->full[s], 1);
+            mbar_init(&bar->empty[s], 1);
+        }
+        mbar_init(&bar->acc_full[0], 1);
+        mbar_init(&bar->acc_empty[0], kEpiThreads);
+        mbar_init(&bar->drain, 1);
+        bar->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) tmem_alloc(&bar->tmem_base, kMxTmemCols);
+    if (warp == 2) {
+        // group row offsets and the prefix sum of their 128-row tile counts
+        int carry = 0;
+        for (int base = 0; base < G; base += 32) {
+            const int g = base + lane;
+            int o0 = 0, o1 = 0;
+            if (g < G) {
+                o0 = p.m_offsets ? p.m_offsets[g] : 0;
+                o1 = p.m_offsets ? p.m_offsets[g + 1] : p.M;
+                offs[g] = o0;
+            }
+            int cnt = (g < G) ? (o1 - o0 + BM - 1) / BM : 0;
+            if (cnt < 0) cnt = 0;
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (g < G) pfx[g] = carry + incl - cnt;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            pfx[G] = carry;
+            offs[G] = p.m_offsets ? p.m_offsets[G] : p.M;
+            bar->num_mtiles = carry;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar->tmem_base;
+    const int KB = p.K / BK;
+    const int num_tiles = bar->num_mtiles * p.tiles_n;
+    const uint32_t sf_col0 = 256;  // TMEM columns [256, 256 + 16*kMxStages): scale factors
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t fills[kMxStages] = {0, 0, 0, 0};
+            bool ok = true;
+            const int64_t atoms_k = p.K / 128;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                const TileCoord c = mx_tile(tile, p.tiles_n, pfx, offs, G);
+                const int brow0 = c.g * p.N + c.tn * kMxBN;
+                const bool two_b_atoms = c.tn * kMxBN + 128 < p.N;
+                const uint32_t bytes = kMxStageBytes + 512u + (two_b_atoms ? 1024u : 512u);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait_bounded(&bar->empty[s], ph ^ 1, abort, p.st, 11)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* stage = smem + s * kMxStageBytes;
+                    uint8_t* sfs = sf + s * kSfStageBytes;
+                    mbar_arrive_expect_tx(&bar->full[s], bytes);
+                    tma_load_2d(stage, &tmA, &bar->full[s], kb * BK, c.row0);
+                    tma_load_2d(stage + BM * BK, &tmB, &bar->full[s], kb * BK, brow0);
+                    bulk_load(sfs, p.sfa + ((int64_t)c.mt_global * atoms_k + kb) * 512, 512, &bar->full[s]);
+                    bulk_load(sfs + 512, p.sfb + ((int64_t)(brow0 / 128) * atoms_k + kb) * 512, 512, &bar->full[s]);
+                    if (two_b_atoms)
+                        bulk_load(sfs + 1024, p.sfb + ((int64_t)(brow0 / 128 + 1) * atoms_k + kb) * 512, 512,
+                                  &bar->full[s]);
+                    ++fills[s];
+                    if (++s == kMxStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok)
+                for (int i = 0; i < kMxStages; ++i)
+                    if (fills[i]) mbar_wait_drain(&bar->full[i], (fills[i] - 1) & 1, p.st);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                if (!mbar_wait_bounded(&bar->acc_empty[0], aph ^ 1, abort, p.st, 12)) break;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait_bounded(&bar->full[s], ph, abort, p.st, 13)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + s * kMxStageBytes);
+                    const uint32_t sf_addr = smem_u32(sf + s * kSfStageBytes);
+                    const uint32_t tsfa = tmem + sf_col0 + 16u * s;
+                    const uint32_t tsfb = tsfa + 4;
+                    tc_cp_32x128b_warpx4(tsfa, sdesc_sf_32x16(sf_addr));
+                    tc_cp_32x128b_warpx4(tsfb, sdesc_sf_32x16(sf_addr + 512));
+                    tc_cp_32x128b_warpx4(tsfb + 4, sdesc_sf_32x16(sf_addr + 1024));
+                    const uint64_t adesc = sdesc_k_sw128(a_addr);
+                    const uint64_t bdesc = sdesc_k_sw128(a_addr + BM * BK);
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        tc_mma_mxf8f6f4(tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8f6f4(BM, kMxBN, k, k), tsfa, tsfb,
+                                        (kb > 0 || k > 0) ? 1u : 0u);
+                    tc_commit(&bar->empty[s]);
+                    if (++s == kMxStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&bar->acc_full[0]);
+                aph ^= 1;
+            }
+            tc_commit(&bar->drain);
+            mbar_wait_drain(&bar->drain, 0, p.st);
+        }
+    } else if (warp >= kEpiWarp0) {
+        const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
+        const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
+        const int64_t q_atoms_k = (p.N + 127) / 128;
+        uint32_t aph = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const TileCoord c = mx_tile(tile, p.tiles_n, pfx, offs, G);
+            const int rl = 32 * q + lane;
+            const int ncol0 = c.tn * kMxBN + 128 * h;
+            const bool mvalid = rl < c.rows, hvalid = ncol0 < p.N;
+            if (!mbar_wait_bounded(&bar->acc_full[0], aph, abort, p.st, 14)) break;
+            tc_fence_after();
+            // two halves of 64 columns: load, wait, round to bf16
+            uint32_t packed[64];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r0[32], r1[32];
+                ld_chunk(tb + 64 * half, r0);
+                ld_chunk(tb + 64 * half + 32, r1);
+                tmem_ld_wait();
+                reg_fence32(r0);
+                reg_fence32(r1);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    packed[32 * half + j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+                    packed[32 * half + 16 + j] =
+                        pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bar->acc_empty[0]);
+            aph ^= 1;
+            const int64_t m = (int64_t)c.row0 + rl;
+            if (mvalid && hvalid) {
+                uint16_t* d = p.D + m * p.ldd + ncol0;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (ncol0 + 8 * i < p.N)
+                        reinterpret_cast<uint4*>(d)[i] =
+                            make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                if (p.q_codes != nullptr) {
+                    const uint32_t sc = quant_row_mx(packed, p.q_codes + m * p.N + ncol0);
+                    *reinterpret_cast<uint32_t*>(p.q_scales + mx_scale_offset(m, ncol0 / 32, q_atoms_k)) = sc;
+                }
+            } else if (p.q_codes != nullptr && hvalid && m < ((int64_t)p.M + 127) / 128 * 128) {
+                // padding rows of the last scale atom row: zero, as the standalone quantizer writes
+                *reinterpret_cast<uint32_t*>(p.q_scales + mx_scale_offset(m, ncol0 / 32, q_atoms_k)) = 0u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kMxTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2-D u8 tensor map over a row-major [rows][cols] matrix with a
+// box of box_rows x 128 bytes and 128-byte swizzle; out-of-range rows read 0.
+bool make_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_blockwise(const GemmBlockwiseArgs& a, StatusBlock* status, cudaStream_t st) {
+    if (a.M == 0 || a.N == 0) return cudaSuccess;
+    CUtensorMap tmA, tmB;
+    if (!make_map(&tmA, a.a_codes, (uint64_t)a.K, (uint64_t)a.M, BM) ||
+        !make_map(&tmB, a.b_codes, (uint64_t)a.K, (uint64_t)a.N, kBwBN))
+        return cudaErrorInvalidValue;
+    BwParams p;
+    p.sa = a.sa;
+    p.sb = a.sb;
+    p.sb_per_row = a.sb_per_row;
+    p.M = (int)a.M;
+    p.N = (int)a.N;
+    p.K = (int)a.K;
+    p.D = a.D;
+    p.ldd = a.ldd;
+    p.d_f32 = a.d_f32;
+    p.q_codes = a.q_codes;
+    p.q_scales = a.q_scales;
+    p.st = status;
+    p.tiles_m = (int)((a.M + BM - 1) / BM);
+    p.tiles_n = (int)((a.N + kBwBN - 1) / kBwBN);
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int grid = tiles < sm_count() ? tiles : sm_count();
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_blockwise, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBlockwise);
+    if (e != cudaSuccess) return e;
+    k_gemm_blockwise<<<grid, kThreads, kSmemBlockwise, st>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_mx(const GemmMxArgs& a, StatusBlock* status, cudaStream_t st) {
+    if (a.M == 0 || a.N == 0) return cudaSuccess;
+    CUtensorMap tmA, tmB;
+    if (!make_map(&tmA, a.a_codes, (uint64_t)a.K, (uint64_t)a.M, BM) ||
+        !make_map(&tmB, a.b_codes, (uint64_t)a.K, (uint64_t)a.N * (uint64_t)a.G, kMxBN))
+        return cudaErrorInvalidValue;
+    MxParams p;
+    p.sfa = a.sfa;
+    p.sfb = a.sfb;
+    p.m_offsets = a.m_offsets;
+    p.G = a.G;
+    p.M = (int)a.M;
+    p.N = (int)a.N;
+    p.K = (int)a.K;
+    p.D = reinterpret_cast<uint16_t*>(a.D);
+    p.ldd = a.ldd;
+    p.q_codes = a.q_codes;
+    p.q_scales = a.q_scales;
+    p.st = status;
+    p.tiles_n = (int)((a.N + kMxBN - 1) / kMxBN);
+    // upper bound of the tile count (the exact count depends on device-side offsets)
+    const int64_t mtiles = a.m_offsets ? (a.M + BM - 1) / BM + a.G : (a.M + BM - 1) / BM;
+    const int64_t tiles = mtiles * p.tiles_n;
+    const int grid = tiles < sm_count() ? (int)tiles : sm_count();
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_mx, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMx);
+    if (e != cudaSuccess) return e;
+    k_gemm_mx<<<grid, kThreads, kSmemMx, st>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8bs

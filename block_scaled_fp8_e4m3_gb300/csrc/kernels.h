@@ -1,0 +1,73 @@
+// kernels.h -- launchers of the device kernels, called by the C-ABI layer
+// (api.cu) after it has validated every argument.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp8bs {
+
+struct StatusBlock;
+
+// quantize.cu
+cudaError_t launch_quant_group_k(const uint16_t* x, int64_t M, int64_t K, int64_t ld, uint8_t* codes,
+                                 float* scales, cudaStream_t st);
+cudaError_t launch_quant_group_m(const uint16_t* x, int64_t M, int64_t K, int64_t ld, uint8_t* codes_t,
+                                 float* scales, cudaStream_t st);
+cudaError_t launch_quant_block(const uint16_t* w, int64_t N, int64_t K, int64_t ld, uint8_t* codes,
+                               float* scales, uint8_t* codes_t, float* scales_t, cudaStream_t st);
+cudaError_t launch_quant_mx(const uint16_t* x, int64_t R, int64_t K, int64_t ld, uint8_t* codes, uint8_t* scales,
+                            cudaStream_t st);
+cudaError_t launch_permute_rows_mx(const uint8_t* src_codes, const uint8_t* src_scales, int64_t src_rows,
+                                   int64_t K, const int32_t* gather, const int32_t* offsets, int32_t G,
+                                   int64_t total, uint8_t* dst_codes, uint8_t* dst_scales, int64_t dst_scale_bytes,
+                                   StatusBlock* status, cudaStream_t st);
+
+// gemm.cu
+struct GemmBlockwiseArgs {
+    const uint8_t* a_codes;  // [M][K]
+    const uint8_t* b_codes;  // [N][K]
+    const float* sa;         // [K/128][M]
+    const float* sb;         // per-block [N/128][K/128] or per-row [K/128][N]
+    int sb_per_row;          // 1 for WGRAD (B quantized 128x1)
+    int64_t M, N, K;
+    void* D;
+    int64_t ldd;
+    int d_f32;
+    uint8_t* q_codes;        // fused 1x128 quantization of D (nullable)
+    float* q_scales;
+};
+cudaError_t launch_gemm_blockwise(const GemmBlockwiseArgs& a, StatusBlock* status, cudaStream_t st);
+
+struct GemmMxArgs {
+    const uint8_t* a_codes;    // [rows_a][K]
+    const uint8_t* b_codes;    // [G*N][K]
+    const uint8_t* sfa;        // MX atoms (grouped layout when m_offsets != nullptr)
+    const uint8_t* sfb;        // MX atoms of the B stack
+    int64_t M;                 // rows of A (total rows when grouped)
+    int64_t N, K;
+    const int32_t* m_offsets;  // device [G+1] or nullptr (single group of M rows)
+    int32_t G;
+    void* D;                   // bf16 [rows][ldd]
+    int64_t ldd;
+    uint8_t* q_codes;          // fused MX quantization of D (nullable; single group only)
+    uint8_t* q_scales;
+};
+cudaError_t launch_gemm_mx(const GemmMxArgs& a, StatusBlock* status, cudaStream_t st);
+
+// sync.cu
+constexpr int kMaxCopySegs = 32;
+struct CopySeg {
+    const uint8_t* src;
+    uint8_t* dst;
+    uint64_t bytes;   // bytes copied from src
+    uint64_t padded;  // bytes written at dst (zero fill after `bytes`); multiple of 16
+    uint64_t dst_word0;  // payload word index of dst[0] (pack: checksum position)
+};
+cudaError_t launch_sync_pack(const CopySeg* segs, int n, unsigned long long* checksum_field, cudaStream_t st);
+cudaError_t launch_sync_verify(const uint8_t* payload, uint64_t data_offset, uint64_t total_bytes,
+                               unsigned long long table_sum, StatusBlock* status, cudaStream_t st);
+cudaError_t launch_sync_scatter(const CopySeg* segs, int n, const StatusBlock* status, cudaStream_t st);
+
+}  // namespace fp8bs

@@ -1,0 +1,391 @@
+// quantize.cu -- HBM-streaming quantizers (bf16 -> E4M3 codes + scales).
+//
+// Every kernel reads each bf16 element once with 16-byte coalesced loads,
+// reduces the group maximum on chip (warp shuffles, or shared memory for
+// groups that span warps), encodes with the hardware round-to-nearest-even
+// saturating E4M3 conversion, and writes codes and scales once.  Algorithmic
+// traffic: 2 B read + 1 B code per element + the scales.
+//
+// Scale conventions (see fp8bs.h): blockwise s = amax/448 by IEEE fp32
+// division and codes from the IEEE fp32 quotient x/s ("AIS: Adaptive
+// Importance Sampling for Quantized RL" explainer, equation Q(X)); MX
+// e = floor(log2 amax) - 8 read from the exponent bits and codes from the
+// exact product x * 2^-e.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8bs {
+
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ float amax8(const float (&f)[8]) {
+    float a = fabsf(f[0]);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) a = fmaxf(a, fabsf(f[i]));
+    return a;
+}
+
+// 8 values divided by s (IEEE) and encoded; returns 8 codes as two words.
+__device__ __forceinline__ uint2 encode8_div(const float (&f)[8], float s) {
+    uint2 r;
+    r.x = e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) | (e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
+    r.y = e4m3x2(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s)) | (e4m3x2(__fdiv_rn(f[6], s), __fdiv_rn(f[7], s)) << 16);
+    return r;
+}
+
+__device__ __forceinline__ uint2 encode8_mul(const float (&f)[8], float m) {
+    uint2 r;
+    r.x = e4m3x2(__fmul_rn(f[0], m), __fmul_rn(f[1], m)) | (e4m3x2(__fmul_rn(f[2], m), __fmul_rn(f[3], m)) << 16);
+    r.y = e4m3x2(__fmul_rn(f[4], m), __fmul_rn(f[5], m)) | (e4m3x2(__fmul_rn(f[6], m), __fmul_rn(f[7], m)) << 16);
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// 1x128 groups along K.  Block = 256 threads = 16 rows (a half-warp per row,
+// 8 bf16 per lane) x 4 consecutive groups; the four 16-byte loads of a
+// thread are issued before any arithmetic.
+// ---------------------------------------------------------------------------
+constexpr int kGK_Groups = 4;
+
+__global__ void __launch_bounds__(256) k_quant_group_k(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                       int64_t ld, uint8_t* __restrict__ codes,
+                                                       float* __restrict__ scales) {
+    const int64_t G = K / 128;
+    const int64_t gchunks = (G + kGK_Groups - 1) / kGK_Groups;
+    const int64_t strip = (int64_t)blockIdx.x / gchunks;
+    const int64_t g0 = ((int64_t)blockIdx.x % gchunks) * kGK_Groups;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane & 15;
+    const int64_t row = strip * 16 + warp * 2 + (lane >> 4);
+    const bool row_ok = row < M;
+
+    uint4 v[kGK_Groups];
+#pragma unroll
+    for (int u = 0; u < kGK_Groups; ++u) {
+        const int64_t g = g0 + u;
+        v[u] = (row_ok && g < G) ? ld_stream_v4(x + row * ld + g * 128 + sub * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kGK_Groups; ++u) {
+        const int64_t g = g0 + u;
+        float f[8];
+        unpack8(v[u], f);
+        float a = amax8(f);
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        const float s = group_scale(a);
+        if (row_ok && g < G) {
+            const uint2 c = encode8_div(f, s);
+            *reinterpret_cast<uint2*>(codes + row * K + g * 128 + sub * 8) = c;
+            if (sub == 0) scales[g * M + row] = s;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 128x1 groups along M, codes transposed.  Block = one 128-row x 64-column
+// tile; thread (chunk = t%8, quad = t/8) holds rows 4*quad..4*quad+3 of
+// columns 8*chunk..8*chunk+7.  Column maxima: in-thread over 4 rows, shuffle
+// over the 4 quads of a warp, shared memory over the 8 warps.  The codes of
+// a column's 4 rows form one 32-bit word of the transposed tile in shared
+// memory (column stride 33 words), which is written out 16 bytes per thread.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_quant_group_m(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                       int64_t ld, uint8_t* __restrict__ codes_t,
+                                                       float* __restrict__ scales) {
+    __shared__ float red[8][64];
+    __shared__ float col_scale[64];
+    __shared__ uint32_t tile[64 * 33];
+
+    const int64_t ctiles = (K + 63) / 64;
+    const int64_t mb = (int64_t)blockIdx.x / ctiles;
+    const int64_t c0 = ((int64_t)blockIdx.x % ctiles) * 64;
+    const int64_t m0 = mb * 128;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int chunk = t & 7, quad = t >> 3;
+    const bool col_ok = c0 + chunk * 8 < K;  // K % 8 == 0: a chunk is all valid or all invalid
+
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        v[i] = col_ok ? ld_stream_v4(x + (m0 + quad * 4 + i) * ld + c0 + chunk * 8) : make_uint4(0, 0, 0, 0);
+
+    float f[4][8];
+    float pa[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) unpack8(v[i], f[i]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float a = fmaxf(fmaxf(fabsf(f[0][j]), fabsf(f[1][j])), fmaxf(fabsf(f[2][j]), fabsf(f[3][j])));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
+        pa[j] = a;
+    }
+    if (lane < 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) red[warp][chunk * 8 + j] = pa[j];
+    }
+    __syncthreads();
+    if (t < 64) {
+        float a = red[0][t];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w][t]);
+        const float s = group_scale(a);
+        col_scale[t] = s;
+        if (c0 + t < K) scales[mb * K + c0 + t] = s;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float s = col_scale[chunk * 8 + j];
+        const uint32_t lo = e4m3x2(__fdiv_rn(f[0][j], s), __fdiv_rn(f[1][j], s));
+        const uint32_t hi = e4m3x2(__fdiv_rn(f[2][j], s), __fdiv_rn(f[3][j], s));
+        tile[(chunk * 8 + j) * 33 + quad] = lo | (hi << 16);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int idx = t + 256 * i;
+        const int col = idx >> 3, part = idx & 7;
+        if (c0 + col < K) {
+            uint4 o;
+            o.x = tile[col * 33 + part * 4 + 0];
+            o.y = tile[col * 33 + part * 4 + 1];
+            o.z = tile[col * 33 + part * 4 + 2];
+            o.w = tile[col * 33 + part * 4 + 3];
+            *reinterpret_cast<uint4*>(codes_t + (c0 + col) * M + m0 + part * 16) = o;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 128x128 blocks.  Block = one weight block; thread (chunk = t%16, rg = t/16)
+// holds rows 8rg..8rg+7 of columns 8chunk..8chunk+7 (eight 16-byte loads in
+// flight).  The block maximum is a warp shuffle reduction followed by a
+// shared-memory reduction over the 8 warps.  The optional transposed copy
+// goes through a shared-memory tile (row stride 144 B) read column-wise; each
+// thread writes 32 contiguous transposed bytes (one full sector).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_quant_block(const uint16_t* __restrict__ w, int64_t N, int64_t K,
+                                                     int64_t ld, uint8_t* __restrict__ codes,
+                                                     float* __restrict__ scales, uint8_t* __restrict__ codes_t,
+                                                     float* __restrict__ scales_t) {
+    constexpr int kStride = 144;
+    __shared__ float red[8];
+    __shared__ __align__(16) uint8_t tile[128 * kStride];
+
+    const int64_t KB = K / 128, NB = N / 128;
+    const int64_t nb = (int64_t)blockIdx.x / KB, kb = (int64_t)blockIdx.x % KB;
+    const int64_t n0 = nb * 128, k0 = kb * 128;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int chunk = t & 15, rg = t >> 4;
+
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = ld_stream_v4(w + (n0 + rg * 8 + i) * ld + k0 + chunk * 8);
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float f[8];
+        unpack8(v[i], f);
+        a = fmaxf(a, amax8(f));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (lane == 0) red[warp] = a;
+    __syncthreads();
+    a = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) a = fmaxf(a, red[i]);
+    const float s = group_scale(a);
+    if (t == 0) {
+        scales[nb * KB + kb] = s;
+        if (scales_t) scales_t[kb * NB + nb] = s;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float f[8];
+        unpack8(v[i], f);
+        const uint2 c = encode8_div(f, s);
+        *reinterpret_cast<uint2*>(codes + (n0 + rg * 8 + i) * K + k0 + chunk * 8) = c;
+        if (codes_t) *reinterpret_cast<uint2*>(tile + (rg * 8 + i) * kStride + chunk * 8) = c;
+    }
+    if (codes_t == nullptr) return;
+    __syncthreads();
+    const int col = t & 127, half = t >> 7;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+        const int r0 = half * 64 + part * 32;
+        uint32_t wds[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            uint32_t wd = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) wd |= (uint32_t)tile[(r0 + q * 4 + b) * kStride + col] << (8 * b);
+            wds[q] = wd;
+        }
+        uint4* dst = reinterpret_cast<uint4*>(codes_t + (k0 + col) * N + n0 + r0);
+        dst[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+        dst[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// MX 1x32 blocks.  Block = one 128-row x 128-column tile, i.e. exactly one
+// 512-byte scale atom; thread (chunk = t%16, slot = t/16) holds rows
+// slot + 16i (i < 8) of columns 8chunk..8chunk+7.  A 32-block spans 4 lanes
+// (shuffle over xor 1, 2).  The atom is assembled in shared memory and
+// written with 16-byte stores.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_quant_mx(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ld,
+                                                  uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    __shared__ __align__(16) uint8_t atom[512];
+    const int64_t atoms_k = (K + 127) / 128;
+    const int64_t rt = (int64_t)blockIdx.x / atoms_k, ct = (int64_t)blockIdx.x % atoms_k;
+    const int64_t r0 = rt * 128, k0 = ct * 128;
+    const int t = threadIdx.x, chunk = t & 15, slot = t >> 4;
+    const int j = chunk >> 2;                     // 32-block inside the atom
+    const bool col_ok = k0 + chunk * 8 < K;      // K % 32 == 0: whole 32-blocks valid or not
+
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t r = r0 + slot + 16 * i;
+        v[i] = (col_ok && r < R) ? ld_stream_v4(x + r * ld + k0 + chunk * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int rl = slot + 16 * i;
+        const int64_t r = r0 + rl;
+        float f[8];
+        unpack8(v[i], f);
+        float a = amax8(f);
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        const int e = mx_exponent(a);
+        if ((chunk & 3) == 0) atom[(rl & 31) * 16 + (rl >> 5) * 4 + j] = (uint8_t)(e + 127);
+        if (col_ok && r < R) {
+            const uint2 c = encode8_mul(f, exp2_int(-e));
+            *reinterpret_cast<uint2*>(codes + r * K + k0 + chunk * 8) = c;
+        }
+    }
+    __syncthreads();
+    if (t < 32)
+        reinterpret_cast<uint4*>(scales + (rt * atoms_k + ct) * 512)[t] = reinterpret_cast<const uint4*>(atom)[t];
+}
+
+// ---------------------------------------------------------------------------
+// MoE row gather of MX codes and scales into expert-contiguous groups.  One
+// warp per destination row: 16-byte code copies, then one 32-bit word per
+// 128-column atom (the 4 scale bytes of a row inside an atom are adjacent).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_permute_rows_mx(const uint8_t* __restrict__ src_codes,
+                                                         const uint8_t* __restrict__ src_scales, int64_t src_rows,
+                                                         int64_t K, const int32_t* __restrict__ gather,
+                                                         const int32_t* __restrict__ offsets, int32_t G,
+                                                         int64_t total, uint8_t* __restrict__ dst_codes,
+                                                         uint8_t* __restrict__ dst_scales, StatusBlock* status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t i = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (i >= total) return;
+    const int64_t src = gather[i];
+    if (src < 0 || src >= src_rows) {
+        if (lane == 0) atomicOr(&status->error_bits, kErrDeviceArg);
+        return;
+    }
+    // group of row i: last g with offsets[g] <= i
+    int lo = 0, hi = G;  // invariant offsets[lo] <= i < offsets[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (offsets[mid] <= i) lo = mid; else hi = mid;
+    }
+    const int g = lo;
+    // atom-row base of group g: sum over h < g of ceil(M_h / 128)
+    int64_t pg = 0;
+    for (int h = lane; h < g; h += 32) pg += (offsets[h + 1] - offsets[h] + 127) / 128;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pg += __shfl_xor_sync(0xffffffffu, pg, o);
+    const int64_t l = i - offsets[g];
+
+    const uint4* s4 = reinterpret_cast<const uint4*>(src_codes + src * K);
+    uint4* d4 = reinterpret_cast<uint4*>(dst_codes + i * K);
+    for (int64_t c = lane; c < K / 16; c += 32) d4[c] = s4[c];
+
+    const int64_t atoms_k = K / 128;
+    const int64_t s_in = (src & 31) * 16 + ((src & 127) >> 5) * 4;
+    const int64_t d_in = (l & 31) * 16 + ((l & 127) >> 5) * 4;
+    const int64_t d_row = pg + (l >> 7);
+    for (int64_t a = lane; a < atoms_k; a += 32) {
+        const uint32_t wd = *reinterpret_cast<const uint32_t*>(src_scales + ((src >> 7) * atoms_k + a) * 512 + s_in);
+        *reinterpret_cast<uint32_t*>(dst_scales + (d_row * atoms_k + a) * 512 + d_in) = wd;
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Launchers (argument checks are done by the API layer).
+// ---------------------------------------------------------------------------
+cudaError_t launch_quant_group_k(const uint16_t* x, int64_t M, int64_t K, int64_t ld, uint8_t* codes,
+                                 float* scales, cudaStream_t st) {
+    if (M == 0) return cudaSuccess;
+    const int64_t G = K / 128;
+    const int64_t blocks = ((M + 15) / 16) * ((G + kGK_Groups - 1) / kGK_Groups);
+    k_quant_group_k<<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ld, codes, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_group_m(const uint16_t* x, int64_t M, int64_t K, int64_t ld, uint8_t* codes_t,
+                                 float* scales, cudaStream_t st) {
+    if (M == 0 || K == 0) return cudaSuccess;
+    const int64_t blocks = (M / 128) * ((K + 63) / 64);
+    k_quant_group_m<<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ld, codes_t, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_block(const uint16_t* w, int64_t N, int64_t K, int64_t ld, uint8_t* codes,
+                               float* scales, uint8_t* codes_t, float* scales_t, cudaStream_t st) {
+    if (N == 0 || K == 0) return cudaSuccess;
+    const int64_t blocks = (N / 128) * (K / 128);
+    k_quant_block<<<(unsigned)blocks, 256, 0, st>>>(w, N, K, ld, codes, scales, codes_t, scales_t);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_mx(const uint16_t* x, int64_t R, int64_t K, int64_t ld, uint8_t* codes, uint8_t* scales,
+                            cudaStream_t st) {
+    if (R == 0 || K == 0) return cudaSuccess;
+    const int64_t blocks = ((R + 127) / 128) * ((K + 127) / 128);
+    k_quant_mx<<<(unsigned)blocks, 256, 0, st>>>(x, R, K, ld, codes, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute_rows_mx(const uint8_t* src_codes, const uint8_t* src_scales, int64_t src_rows,
+                                   int64_t K, const int32_t* gather, const int32_t* offsets, int32_t G,
+                                   int64_t total, uint8_t* dst_codes, uint8_t* dst_scales, int64_t dst_scale_bytes,
+                                   StatusBlock* status, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(dst_scales, 0, (size_t)dst_scale_bytes, st);
+    if (e != cudaSuccess || total == 0) return e;
+    const int64_t blocks = (total + 7) / 8;
+    k_permute_rows_mx<<<(unsigned)blocks, 256, 0, st>>>(src_codes, src_scales, src_rows, K, gather, offsets, G, total,
+                                                        dst_codes, dst_scales, status);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8bs

@@ -1,0 +1,191 @@
+"""GPU parity of the block-scaled GEMMs against the oracle's fp64 product of
+the dequantized operands, within |gpu - ref| <= 2e-3 sum|ab| + 2^-8 |ref|.
+Operands are quantized on the GPU (byte-equal to the oracle, checked in
+test_gpu_quant) and independently by the oracle from the same bf16 inputs."""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_fp8_e4m3_gb300 as fp8
+import oracle
+from block_scaled_fp8_e4m3_gb300 import synth
+from gpu_util import (DEV, assert_bytes_equal, assert_gemm_close, bf16_dev_to_f64, oracle_block, oracle_group_k,
+                      oracle_group_m, oracle_mx, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+def _fwd_case(M, N, K, seed):
+    X = synth.random_bf16((M, K), seed=seed, outliers=True)
+    W = synth.random_bf16((N, K), seed=seed + 1000, std=0.02)
+    return X, W
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (300, 512, 512), (1, 128, 256), (257, 384, 1024),
+                                   (640, 1280, 384)])
+def test_blockwise_fwd(M, N, K):
+    X, W = _fwd_case(M, N, K, seed=M + N + K)
+    qx = fp8.quantize_group(X.to(DEV), "K")
+    qw = fp8.quantize_block(W.to(DEV))
+    Y = fp8.gemm(qx, qw, "fwd")
+    cx, sx = oracle_group_k(X)
+    cw, sw = oracle_block(W)
+    ref, mag = oracle.gemm_ref(oracle.dequant_group(cx, sx), oracle.dequant_block(cw, sw))
+    assert_gemm_close(bf16_dev_to_f64(Y), ref, mag, f"fwd {M}x{N}x{K}")
+
+
+def test_blockwise_fwd_f32_out_and_fused_quant():
+    M, N, K = 200, 512, 640
+    X, W = _fwd_case(M, N, K, seed=77)
+    qx = fp8.quantize_group(X.to(DEV), "K")
+    qw = fp8.quantize_block(W.to(DEV))
+    Y32 = fp8.gemm(qx, qw, "fwd", out_dtype=torch.float32)
+    Y, qy = fp8.gemm(qx, qw, "fwd", quantize_output=True)
+    cx, sx = oracle_group_k(X)
+    cw, sw = oracle_block(W)
+    ref, mag = oracle.gemm_ref(oracle.dequant_group(cx, sx), oracle.dequant_block(cw, sw))
+    assert_gemm_close(Y32.double().cpu().numpy(), ref, mag, "fwd f32")
+    assert_gemm_close(bf16_dev_to_f64(Y), ref, mag, "fwd bf16")
+    # the fused quantization equals the standalone quantizer applied to Y
+    q2 = fp8.quantize_group(Y, "K")
+    assert_bytes_equal(to_np(qy.codes), to_np(q2.codes), "fused codes")
+    assert_bytes_equal(to_np(qy.scales), to_np(q2.scales), "fused scales")
+    # and the oracle's quantization of the returned bf16 Y
+    c, s = oracle_group_k(Y.cpu())
+    assert_bytes_equal(to_np(qy.codes), c, "fused codes vs oracle")
+
+
+@pytest.mark.parametrize("M,Nw,Kw", [(256, 256, 384), (384, 512, 256)])
+def test_dgrad_wgrad(M, Nw, Kw):
+    """dX = dY W  (A = dY 1x128, B = W^T 128x128 transposed copy) and
+    dW = dY^T X (A = dY^T, B = X^T, both from 128x1 groups)."""
+    dY = synth.random_bf16((M, Nw), seed=M + 1, std=1e-3)
+    W = synth.random_bf16((Nw, Kw), seed=M + 2, std=0.02)
+    X = synth.random_bf16((M, Kw), seed=M + 3, outliers=True)
+    q_dy = fp8.quantize_group(dY.to(DEV), "K")
+    _, q_wt = fp8.quantize_block(W.to(DEV), transposed=True)
+    dX = fp8.gemm(q_dy, q_wt, "dgrad")
+    c_dy, s_dy = oracle_group_k(dY)
+    _, _, c_wt, s_wt = oracle_block(W, transposed=True)
+    ref, mag = oracle.gemm_ref(oracle.dequant_group(c_dy, s_dy), oracle.dequant_block(c_wt, s_wt))
+    assert_gemm_close(bf16_dev_to_f64(dX), ref, mag, "dgrad")
+
+    q_dyt = fp8.quantize_group(dY.to(DEV), "M")
+    q_xt = fp8.quantize_group(X.to(DEV), "M")
+    for dt in (torch.bfloat16, torch.float32):
+        dW = fp8.gemm(q_dyt, q_xt, "wgrad", out_dtype=dt)
+        c1, s1 = oracle_group_m(dY)
+        c2, s2 = oracle_group_m(X)
+        ref, mag = oracle.gemm_ref(oracle.dequant_group(c1, s1), oracle.dequant_group(c2, s2))
+        assert_gemm_close(dW.double().cpu().numpy(), ref, mag, f"wgrad {dt}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (300, 512, 512), (1, 256, 256), (200, 400, 384),
+                                   (513, 1024, 1024)])
+def test_mx_fwd(M, N, K):
+    X, W = _fwd_case(M, N, K, seed=M * 3 + N + K)
+    qx = fp8.quantize_mx(X.to(DEV))
+    qw = fp8.quantize_mx(W.to(DEV))
+    Y = fp8.gemm(qx, qw, "fwd")
+    cx, sx = oracle_mx(X)
+    cw, sw = oracle_mx(W)
+    ref, mag = oracle.gemm_ref(oracle.dequant_mx(cx, sx), oracle.dequant_mx(cw, sw))
+    assert_gemm_close(bf16_dev_to_f64(Y), ref, mag, f"mx {M}x{N}x{K}")
+
+
+def test_mx_fused_quant():
+    M, N, K = 300, 512, 256
+    X, W = _fwd_case(M, N, K, seed=91)
+    qx = fp8.quantize_mx(X.to(DEV))
+    qw = fp8.quantize_mx(W.to(DEV))
+    Y, qy = fp8.gemm(qx, qw, "fwd", quantize_output=True)
+    q2 = fp8.quantize_mx(Y)
+    assert_bytes_equal(to_np(qy.codes), to_np(q2.codes), "fused codes")
+    assert_bytes_equal(to_np(qy.scales), to_np(q2.scales), "fused scales")
+
+
+def test_mx_scale_factors_are_applied_per_row_and_block():
+    """Structured operands: A codes all 1.0 with scale 2^(r%7 - 3) varying by
+    row and 32-block; B codes 1.0 with scale 2^(n%5 - 2).  D is then a
+    closed form sum over blocks of products of powers of two."""
+    M, N, K = 256, 256, 256
+    a = torch.ones((M, K))
+    for kb in range(K // 32):
+        a[:, kb * 32:(kb + 1) * 32] *= torch.exp2(((torch.arange(M) + kb) % 7 - 3).float())[:, None]
+    b = torch.ones((N, K))
+    for kb in range(K // 32):
+        b[:, kb * 32:(kb + 1) * 32] *= torch.exp2(((torch.arange(N) * 3 + kb) % 5 - 2).float())[:, None]
+    A, B = a.to(torch.bfloat16), b.to(torch.bfloat16)
+    Y = fp8.gemm(fp8.quantize_mx(A.to(DEV)), fp8.quantize_mx(B.to(DEV)))
+    exact = a.double() @ b.double().T
+    assert torch.equal(Y.double().cpu(), exact.to(torch.bfloat16).double())
+
+
+def test_blockwise_scales_closed_form():
+    """Blockwise: every group constant -> D exact: codes 448 at scale amax/448."""
+    M, N, K = 256, 256, 512
+    a = torch.ones((M, K))
+    for g in range(K // 128):
+        a[:, g * 128:(g + 1) * 128] *= torch.exp2(((torch.arange(M) + g) % 5 - 2).float())[:, None]
+    b = torch.ones((N, K))
+    for nb in range(N // 128):
+        for kb in range(K // 128):
+            b[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128] *= 2.0 ** ((nb + 2 * kb) % 3 - 1)
+    qa = fp8.quantize_group(a.to(torch.bfloat16).to(DEV), "K")
+    qb = fp8.quantize_block(b.to(torch.bfloat16).to(DEV))
+    Y = fp8.gemm(qa, qb, out_dtype=torch.float32)
+    exact = a.double() @ b.double().T
+    assert torch.allclose(Y.double().cpu(), exact, rtol=1e-6, atol=0)
+
+
+# ---------------------------------------------------------------- full size, sampled
+def _sampled_check(Y, A_deq, B_deq, what, n=4096, seed=0):
+    rng = np.random.default_rng(seed)
+    M, N = Y.shape
+    ms = rng.integers(0, M, n)
+    ns = rng.integers(0, N, n)
+    # always include the corners and tile edges
+    ms = np.concatenate([ms, [0, M - 1, 127, 128, M - 1]])
+    ns = np.concatenate([ns, [0, N - 1, 255, 256, 0]])
+    ref, mag = oracle.gemm_ref_sampled(A_deq, B_deq, ms, ns)
+    got = Y[torch.from_numpy(ms).to(Y.device), torch.from_numpy(ns).to(Y.device)].double().cpu().numpy()
+    assert_gemm_close(got, ref, mag, what)
+
+
+def test_full_mlp_forward_sampled():
+    wl = synth.mlp()
+    X, W = wl.tensors["X"], wl.tensors["W"]
+    qx = fp8.quantize_group(X.to(DEV), "K")
+    qw = fp8.quantize_block(W.to(DEV))
+    Y, qy = fp8.gemm(qx, qw, "fwd", quantize_output=True)
+    cx, sx = oracle_group_k(X)
+    cw, sw = oracle_block(W)
+    _sampled_check(Y, oracle.dequant_group(cx, sx), oracle.dequant_block(cw, sw), "mlp fwd 8192x4096x12288")
+    q2 = fp8.quantize_group(Y, "K")
+    assert torch.equal(qy.codes, q2.codes) and torch.equal(qy.scales, q2.scales)
+
+
+def test_full_backward_sampled():
+    wl = synth.backward()
+    dY, W, X = wl.tensors["dY"], wl.tensors["W"], wl.tensors["X"]
+    q_dy = fp8.quantize_group(dY.to(DEV), "K")
+    _, q_wt = fp8.quantize_block(W.to(DEV), transposed=True)
+    dX = fp8.gemm(q_dy, q_wt, "dgrad")
+    c_dy, s_dy = oracle_group_k(dY)
+    _, _, c_wt, s_wt = oracle_block(W, transposed=True)
+    _sampled_check(dX, oracle.dequant_group(c_dy, s_dy), oracle.dequant_block(c_wt, s_wt), "dgrad full")
+    q_dyt = fp8.quantize_group(dY.to(DEV), "M")
+    q_xt = fp8.quantize_group(X.to(DEV), "M")
+    dW = fp8.gemm(q_dyt, q_xt, "wgrad")
+    c1, s1 = oracle_group_m(dY)
+    c2, s2 = oracle_group_m(X)
+    _sampled_check(dW, oracle.dequant_group(c1, s1), oracle.dequant_group(c2, s2), "wgrad full")
+
+
+def test_full_mx_sampled():
+    wl = synth.mx()
+    X, W = wl.tensors["X"], wl.tensors["W"]
+    Y = fp8.gemm(fp8.quantize_mx(X.to(DEV)), fp8.quantize_mx(W.to(DEV)))
+    cx, sx = oracle_mx(X)
+    cw, sw = oracle_mx(W)
+    _sampled_check(Y, oracle.dequant_mx(cx, sx), oracle.dequant_mx(cw, sw), "mx full")

@@ -1,0 +1,113 @@
+"""GPU parity of the MoE path: quantize once, gather rows into expert groups
+(bit-exact: equals quantizing the gathered rows), grouped MXFP8 GEMM within
+tolerance per expert segment."""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_fp8_e4m3_gb300 as fp8
+import oracle
+from block_scaled_fp8_e4m3_gb300 import synth
+from gpu_util import DEV, assert_bytes_equal, assert_gemm_close, oracle_mx, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _grouped_oracle_scales(codes_src, scales_src, gather, offsets, K):
+    """Expected grouped-layout scale bytes, by definition: dst row i of group
+    g sits at atom row P_g + (i - off_g)/128, P_g = sum_{h<g} ceil(M_h/128)."""
+    G = len(offsets) - 1
+    P = np.zeros(G + 1, np.int64)
+    for g in range(G):
+        P[g + 1] = P[g] + (offsets[g + 1] - offsets[g] + 127) // 128
+    total = offsets[-1]
+    out = np.zeros(((total + 127) // 128 + G) * (K // 128) * 512, np.uint8)
+    for g in range(G):
+        for i in range(offsets[g], offsets[g + 1]):
+            src = gather[i]
+            l = i - offsets[g]
+            for kb in range(K // 32):
+                out[oracle.mx_scale_offset(P[g] * 128 + l, kb, K)] = scales_src[oracle.mx_scale_offset(src, kb, K)]
+    return out
+
+
+def _moe_case(tokens, experts, top_k, hidden, ffn, seed):
+    wl = synth.moe(tokens=tokens, experts=experts, top_k=top_k, hidden=hidden, ffn=ffn, seed=seed)
+    return wl.tensors["X"], wl.tensors["W"], wl.tensors["gather"], wl.tensors["offsets"]
+
+
+def _run(X, W, gather, offsets):
+    G, N, K = W.shape
+    qx = fp8.quantize_mx(X.to(DEV))
+    qa = fp8.permute_rows_mx(qx, gather.to(DEV), offsets.to(DEV))
+    qw = fp8.quantize_mx(W.reshape(G * N, K).to(DEV))
+    Y = fp8.grouped_gemm(qa, qw, offsets.to(DEV), N)
+    return qa, Y
+
+
+@pytest.mark.parametrize("tokens,experts,top_k,hidden,ffn,seed", [(200, 8, 2, 256, 256, 5),
+                                                                  (700, 16, 4, 512, 512, 6)])
+def test_moe_small(tokens, experts, top_k, hidden, ffn, seed):
+    X, W, gather, offsets = _moe_case(tokens, experts, top_k, hidden, ffn, seed)
+    qa, Y = _run(X, W, gather, offsets)
+    g_np, off_np = gather.numpy(), offsets.numpy().astype(np.int64)
+    cx, sx = oracle_mx(X)
+    # permutation: codes and scales exactly as defined
+    assert_bytes_equal(to_np(qa.codes), cx[g_np], "permuted codes")
+    assert_bytes_equal(to_np(qa.scales), _grouped_oracle_scales(cx, sx, g_np, off_np, hidden), "grouped scales")
+    # quantize-then-permute == permute-then-quantize
+    cp, sp = oracle_mx(X[torch.from_numpy(g_np.astype(np.int64))])
+    assert np.array_equal(cp, cx[g_np])
+    # grouped GEMM per expert segment
+    A_deq = oracle.dequant_mx(cx, sx)[g_np]
+    G, N, K = W.shape
+    cw, sw = oracle_mx(W.reshape(G * N, K))
+    W_deq = oracle.dequant_mx(cw, sw).reshape(G, N, K)
+    Yh = Y.double().cpu().numpy()
+    for g in range(G):
+        a, b = off_np[g], off_np[g + 1]
+        if b == a:
+            continue
+        ref, mag = oracle.gemm_ref(A_deq[a:b], W_deq[g])
+        assert_gemm_close(Yh[a:b], ref, mag, f"expert {g} ({b - a} rows)")
+
+
+def test_moe_empty_and_single_row_groups():
+    """Groups with 0 and 1 rows, and a group that is an exact multiple of 128."""
+    K, N, G = 256, 256, 4
+    counts = [0, 1, 128, 77]
+    offsets = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32)
+    total = int(offsets[-1])
+    X = synth.random_bf16((50, K), seed=3, outliers=True)
+    gather = torch.randint(0, 50, (total,), generator=torch.Generator().manual_seed(4), dtype=torch.int64).to(torch.int32)
+    W = synth.random_bf16((G, N, K), seed=5, std=0.02)
+    qa, Y = _run(X, W, gather, offsets)
+    cx, sx = oracle_mx(X)
+    A_deq = oracle.dequant_mx(cx, sx)[gather.numpy()]
+    cw, sw = oracle_mx(W.reshape(G * N, K))
+    W_deq = oracle.dequant_mx(cw, sw).reshape(G, N, K)
+    off = offsets.numpy()
+    for g in range(G):
+        a, b = off[g], off[g + 1]
+        if b > a:
+            ref, mag = oracle.gemm_ref(A_deq[a:b], W_deq[g])
+            assert_gemm_close(Y[a:b].double().cpu().numpy(), ref, mag, f"group {g}")
+
+
+def test_full_moe_sampled():
+    X, W, gather, offsets = _moe_case(16384, 64, 8, 2048, 1024, 4)
+    qa, Y = _run(X, W, gather, offsets)
+    g_np, off_np = gather.numpy(), offsets.numpy().astype(np.int64)
+    cx, sx = oracle_mx(X)
+    assert_bytes_equal(to_np(qa.codes), cx[g_np], "permuted codes")
+    G, N, K = W.shape
+    cw, sw = oracle_mx(W.reshape(G * N, K))
+    A_deq_src = oracle.dequant_mx(cx, sx)
+    W_deq = oracle.dequant_mx(cw, sw)
+    rng = np.random.default_rng(1)
+    rows = rng.integers(0, off_np[-1], 4096)
+    cols = rng.integers(0, N, 4096)
+    grp = np.searchsorted(off_np, rows, side="right") - 1
+    ref, mag = oracle.gemm_ref_sampled(A_deq_src, W_deq, g_np[rows].astype(np.int64), grp * N + cols)
+    got = Y[torch.from_numpy(rows).to(DEV), torch.from_numpy(cols).to(DEV)].double().cpu().numpy()
+    assert_gemm_close(got, ref, mag, "moe full sampled")

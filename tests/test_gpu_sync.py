@@ -1,0 +1,123 @@
+"""GPU parity of the weight-sync path: the device payload is byte-identical to
+the oracle's, the installed rollout tensors are bit-identical to the
+trainer's, and corruption is caught before anything is written."""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_fp8_e4m3_gb300 as fp8
+import oracle
+from block_scaled_fp8_e4m3_gb300 import synth
+from gpu_util import DEV, assert_bytes_equal, oracle_block, oracle_group_k, oracle_mx, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _trainer_tensors(seed=0, n=384, k=512):
+    W = synth.random_bf16((n, k), seed=seed + 1, std=0.02)
+    X = synth.random_bf16((130, 256), seed=seed + 2, outliers=True)
+    M = synth.random_bf16((100, 96), seed=seed + 3)
+    N = synth.random_bf16((3, 72), seed=seed + 4)
+    return W, X, M, N
+
+
+def _entries(W, X, M, N):
+    qw = fp8.quantize_block(W.to(DEV))
+    qx = fp8.quantize_group(X.to(DEV), "K")
+    qm = fp8.quantize_mx(M.to(DEV))
+    nd = N.to(DEV)
+    return [fp8.SyncEntry(0x1111, qw), fp8.SyncEntry(0x2222, qx), fp8.SyncEntry(0x3333, qm),
+            fp8.SyncEntry(0x4444, nd)]
+
+
+def _oracle_specs(W, X, M, N):
+    cw, sw = oracle_block(W)
+    cx, sx = oracle_group_k(X)
+    cm, sm = oracle_mx(M)
+    return [
+        dict(tag=0x1111, kind=oracle.KIND_FP8, recipe=oracle.RECIPE_BLOCKWISE, rows=W.shape[0], cols=W.shape[1],
+             layout=oracle.LAYOUT_BLOCK_128x128, data=cw, scales=sw),
+        dict(tag=0x2222, kind=oracle.KIND_FP8, recipe=oracle.RECIPE_BLOCKWISE, rows=130, cols=256,
+             layout=oracle.LAYOUT_GROUP_1x128, data=cx, scales=sx),
+        dict(tag=0x3333, kind=oracle.KIND_FP8, recipe=oracle.RECIPE_MX, rows=100, cols=96,
+             layout=oracle.LAYOUT_MX_1x32, data=cm, scales=sm),
+        dict(tag=0x4444, kind=oracle.KIND_BF16, recipe=oracle.RECIPE_NONE, rows=3, cols=72,
+             layout=oracle.LAYOUT_NONE, data=synth.bf16_bits(N), scales=None),
+    ]
+
+
+def _empty_like(entries):
+    out = []
+    for e in entries:
+        t = e.tensor
+        if isinstance(t, fp8.QTensor):
+            t2 = fp8.QTensor(torch.zeros_like(t.codes), torch.zeros_like(t.scales), t.rows, t.cols, t.recipe,
+                             t.layout)
+        else:
+            t2 = torch.zeros_like(t)
+        out.append(fp8.SyncEntry(e.tag, t2))
+    return out
+
+
+def test_payload_matches_oracle_and_round_trip():
+    W, X, M, N = _trainer_tensors()
+    entries = _entries(W, X, M, N)
+    payload = fp8.sync_pack(entries)
+    ref = oracle.sync_pack(_oracle_specs(W, X, M, N))
+    assert_bytes_equal(payload.cpu().numpy(), ref, "payload")
+    dst = _empty_like(entries)
+    fp8.sync_install(payload, dst)
+    for s, d in zip(entries, dst):
+        if isinstance(s.tensor, fp8.QTensor):
+            assert torch.equal(s.tensor.codes, d.tensor.codes)
+            assert torch.equal(s.tensor.scales.view(torch.uint8), d.tensor.scales.view(torch.uint8))
+        else:
+            assert torch.equal(s.tensor.view(torch.int16), d.tensor.view(torch.int16))
+
+
+def test_corrupted_payload_writes_nothing():
+    W, X, M, N = _trainer_tensors(seed=10)
+    entries = _entries(W, X, M, N)
+    payload = fp8.sync_pack(entries).clone()
+    payload[payload.numel() // 2] ^= 0x40                     # a data byte
+    dst = _empty_like(entries)
+    with pytest.raises(fp8.FP8Error) as ei:
+        fp8.sync_install(payload, dst)
+    assert ei.value.status == 5                               # FP8_ERR_CHECKSUM
+    for d in dst:
+        t = d.tensor.codes if isinstance(d.tensor, fp8.QTensor) else d.tensor
+        assert int(t.view(torch.uint8).count_nonzero()) == 0
+    # a clean install afterwards works (the status block was cleared)
+    good = fp8.sync_pack(entries)
+    fp8.sync_install(good, dst)
+
+
+def test_header_mismatch_rejected_on_host():
+    W, X, M, N = _trainer_tensors(seed=20)
+    entries = _entries(W, X, M, N)
+    payload = fp8.sync_pack(entries)
+    dst = _empty_like(entries)
+    dst[1] = fp8.SyncEntry(0x9999, dst[1].tensor)              # wrong tag
+    with pytest.raises(fp8.FP8Error) as ei:
+        fp8.sync_install(payload, dst)
+    assert ei.value.status == 4                               # FP8_ERR_BAD_PAYLOAD
+    with pytest.raises(fp8.FP8Error) as ei:
+        fp8.sync_install(payload, _empty_like(entries)[:3])   # wrong count
+    assert ei.value.status in (4,)
+
+
+def test_full_mlp_weight_round_trip():
+    """The dense-MLP weight (12288x4096, 128x128 blocks): pack -> install is
+    bit-identical, and the payload equals the oracle's byte for byte."""
+    W = synth.mlp().tensors["W"]
+    qw = fp8.quantize_block(W.to(DEV))
+    entries = [fp8.SyncEntry(7, qw)]
+    payload = fp8.sync_pack(entries)
+    cw, sw = oracle_block(W)
+    ref = oracle.sync_pack([dict(tag=7, kind=oracle.KIND_FP8, recipe=oracle.RECIPE_BLOCKWISE, rows=12288,
+                                 cols=4096, layout=oracle.LAYOUT_BLOCK_128x128, data=cw, scales=sw)])
+    assert_bytes_equal(payload.cpu().numpy(), ref, "payload")
+    dst = _empty_like(entries)
+    fp8.sync_install(payload, dst)
+    assert torch.equal(dst[0].tensor.codes, qw.codes)
+    assert torch.equal(dst[0].tensor.scales, qw.scales)
