@@ -1,0 +1,541 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-scaled FP8 hot path on GB300.
+
+One step = one pass of the dense-MLP workload (X [8192,4096] bf16 with 0.1%
+x50 outliers, W [12288,4096] ~N(0,0.02), seed 2):
+  1x128 quantize X -> 128x128 quantize W -> blockwise FP8 GEMM Y = X W^T
+  (fp32 accumulate, bf16 out, 1x128 quantization of Y fused in the epilogue)
+  -> weight-sync pack of W -> install into the rollout copy.
+value = GEMM FLOPs (2 M N K) per step / device time per step, inputs resident
+in HBM; L2 (129 MB) is flushed between steps by writing 256 MB.
+
+Also reported: the dominant kernel's roofline (GEMM against the FP8 dense
+peak = 2 x measured bf16 peak), every kernel's own roofline over all
+workloads ("kernels"), an end-to-end number through the public API with
+host buffers ("e2e"), the CPU oracle on a bounded sample ("cpu_baseline"),
+SM clocks sampled during the timed region, and the kernel launch count.
+
+--impl reference times the CPU oracle (the only reference this project
+has) on a bounded sample of the same workload per step.
+Multi-GPU: replicas only (each rank runs the same independent workload;
+no data-path collective); value sums over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-scaled FP8 GEMM TFLOP/s + quantize GB/s, % of GB300 roofline"
+WORKLOAD = "dense MLP forward + weight sync: X 8192x4096 (1x128), W 12288x4096 (128x128), GEMM 8192x4096x12288"
+M, K, N = 8192, 4096, 12288
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ timing helpers
+class Flusher:
+    def __init__(self, dev):
+        self.buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def time_kernel(fn, flush, reps, warmup=3):
+    """Average device time (ms) of fn() over reps, L2 flushed before each."""
+    for _ in range(warmup):
+        flush()
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in ts]))
+
+
+# ------------------------------------------------------------------ our arm
+def make_step(fp8, X, W, dev):
+    qx = fp8.quantize_group(X, "K")
+    qw = fp8.quantize_block(W)
+    Y, qy = fp8.gemm(qx, qw, "fwd", quantize_output=True)
+    payload = fp8.sync_pack([fp8.SyncEntry(1, qw)])
+    rollout = fp8.QTensor(torch.empty_like(qw.codes), torch.empty_like(qw.scales), qw.rows, qw.cols, qw.recipe,
+                          qw.layout)
+    torch.cuda.synchronize()
+
+    def step(events=None):
+        rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
+        rec(0)
+        fp8.quantize_group(X, "K", out=qx)
+        rec(1)
+        fp8.quantize_block(W, out=qw)
+        rec(2)
+        fp8.gemm(qx, qw, "fwd", quantize_output=True, out=Y, out_q=qy)
+        rec(3)
+        fp8.sync_pack([fp8.SyncEntry(1, qw)], payload=payload)
+        rec(4)
+        fp8.sync_install(payload, [fp8.SyncEntry(1, rollout)], check=False)
+        rec(5)
+        return Y
+
+    return step, payload.numel(), (qx, qw, Y, qy, rollout)
+
+
+KERNELS_PER_STEP = 6   # quant X, quant W, GEMM, pack, install verify + scatter
+
+
+def breakdown(fp8, synth, dev, flush, pk, reps):
+    """Every kernel of the hot path on its own workload, against its roofline."""
+    hbm = pk["hbm_gbs"]
+    fp8_peak = 2.0 * pk["bf16_tflops"]
+    out = {}
+
+    def rec(name, ms, bytes_=None, flops=None, workload=""):
+        d = {"ms": round(ms, 5), "workload": workload}
+        if bytes_ is not None:
+            gbs = bytes_ / (ms * 1e-3) / 1e9
+            d.update(bound="hbm", achieved=round(gbs, 1), unit="GB/s", peak=hbm, frac=round(gbs / hbm, 4),
+                     frac_of_8tbs=round(gbs / 8000.0, 4), algorithmic_bytes=int(bytes_))
+        else:
+            tf = flops / (ms * 1e-3) / 1e12
+            d.update(bound="tensor", achieved=round(tf, 1), unit="TFLOP/s", peak=round(fp8_peak, 1),
+                     frac=round(tf / fp8_peak, 4), algorithmic_flops=int(flops))
+        out[name] = d
+
+    # dense MLP forward + sync
+    wl = synth.mlp()
+    X, W = wl.tensors["X"].to(dev), wl.tensors["W"].to(dev)
+    qx = fp8.quantize_group(X, "K")
+    qw = fp8.quantize_block(W)
+    rec("quant_group_1x128", time_kernel(lambda: fp8.quantize_group(X, "K", out=qx), flush, reps),
+        bytes_=M * K * (3 + 4 / 128), workload="X 8192x4096")
+    rec("quant_block_128x128", time_kernel(lambda: fp8.quantize_block(W, out=qw), flush, reps),
+        bytes_=N * K * (3 + 4 / 16384), workload="W 12288x4096")
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    rec("gemm_blockwise_fwd", time_kernel(lambda: fp8.gemm(qx, qw, out=Y), flush, reps),
+        flops=2.0 * M * N * K, workload="8192x4096x12288")
+    Y2, qy = fp8.gemm(qx, qw, quantize_output=True)
+    rec("gemm_blockwise_fwd_fused_quant",
+        time_kernel(lambda: fp8.gemm(qx, qw, quantize_output=True, out=Y2, out_q=qy), flush, reps),
+        flops=2.0 * M * N * K, workload="8192x4096x12288 + 1x128 quant of Y")
+    payload = fp8.sync_pack([fp8.SyncEntry(1, qw)])
+    rollout = fp8.QTensor(torch.empty_like(qw.codes), torch.empty_like(qw.scales), qw.rows, qw.cols, qw.recipe,
+                          qw.layout)
+    pb = payload.numel()
+    rec("sync_pack", time_kernel(lambda: fp8.sync_pack([fp8.SyncEntry(1, qw)], payload=payload), flush, reps),
+        bytes_=2 * pb, workload=f"W 12288x4096 payload {pb} B")
+    rec("sync_install", time_kernel(lambda: fp8.sync_install(payload, [fp8.SyncEntry(1, rollout)], check=False),
+                                    flush, reps),
+        bytes_=2 * pb, workload=f"W 12288x4096 payload {pb} B")
+    del X, W, qx, qw, Y, Y2, qy, payload, rollout
+    torch.cuda.empty_cache()
+
+    # backward
+    wl = synth.backward()
+    dY, Wb, Xb = (wl.tensors[k].to(dev) for k in ("dY", "W", "X"))
+    q_dy = fp8.quantize_group(dY, "K")
+    q_w, q_wt = fp8.quantize_block(Wb, transposed=True)
+    q_dyt = fp8.quantize_group(dY, "M")
+    q_xt = fp8.quantize_group(Xb, "M")
+    Mb, Nb, Kb = 8192, 4096, 4096
+    rec("quant_group_128x1_T", time_kernel(lambda: fp8.quantize_group(Xb, "M", out=q_xt), flush, reps),
+        bytes_=Mb * Kb * (3 + 4 / 128), workload="X 8192x4096 -> X^T")
+    rec("quant_block_128x128_with_T", time_kernel(lambda: fp8.quantize_block(Wb, True, out=q_w, out_t=q_wt),
+                                                  flush, reps),
+        bytes_=Nb * Kb * (4 + 8 / 16384), workload="W 4096x4096 + transposed copy")
+    dX = torch.empty((Mb, Kb), dtype=torch.bfloat16, device=dev)
+    rec("gemm_blockwise_dgrad", time_kernel(lambda: fp8.gemm(q_dy, q_wt, "dgrad", out=dX), flush, reps),
+        flops=2.0 * Mb * Nb * Kb, workload="dX = dY W, 8192x4096(N)x4096")
+    dW = torch.empty((Nb, Kb), dtype=torch.bfloat16, device=dev)
+    rec("gemm_blockwise_wgrad", time_kernel(lambda: fp8.gemm(q_dyt, q_xt, "wgrad", out=dW), flush, reps),
+        flops=2.0 * Mb * Nb * Kb, workload="dW = dY^T X, 4096x8192(M)x4096")
+    del dY, Wb, Xb, q_dy, q_w, q_wt, q_dyt, q_xt, dX, dW
+    torch.cuda.empty_cache()
+
+    # MXFP8 forward
+    wl = synth.mx()
+    Xm, Wm = wl.tensors["X"].to(dev), wl.tensors["W"].to(dev)
+    qxm, qwm = fp8.quantize_mx(Xm), fp8.quantize_mx(Wm)
+    rec("quant_mx_1x32", time_kernel(lambda: fp8.quantize_mx(Wm, out=qwm), flush, reps),
+        bytes_=4096 * 4096 * (3 + 1 / 32), workload="W 4096x4096")
+    Ym = torch.empty((2048, 4096), dtype=torch.bfloat16, device=dev)
+    rec("gemm_mx_fwd", time_kernel(lambda: fp8.gemm(qxm, qwm, out=Ym), flush, reps),
+        flops=2.0 * 2048 * 4096 * 4096, workload="2048x4096x4096")
+    del Xm, Wm, qxm, qwm, Ym
+    torch.cuda.empty_cache()
+
+    # MoE
+    wl = synth.moe()
+    Xe, We = wl.tensors["X"].to(dev), wl.tensors["W"]
+    G, Ne, Ke = We.shape
+    We = We.reshape(G * Ne, Ke).to(dev)
+    gather, offsets = wl.tensors["gather"].to(dev), wl.tensors["offsets"].to(dev)
+    qxe = fp8.quantize_mx(Xe)
+    qa = fp8.permute_rows_mx(qxe, gather, offsets)
+    qwe = fp8.quantize_mx(We)
+    rows = gather.numel()
+    rec("permute_rows_mx", time_kernel(lambda: fp8.permute_rows_mx(qxe, gather, offsets, out=qa), flush, reps),
+        bytes_=2 * rows * Ke + 4 * rows + 2 * rows * Ke / 32, workload=f"{rows} rows x {Ke}")
+    Ye = torch.empty((rows, Ne), dtype=torch.bfloat16, device=dev)
+    rec("gemm_mx_grouped", time_kernel(lambda: fp8.grouped_gemm(qa, qwe, offsets, Ne, out=Ye), flush, reps),
+        flops=2.0 * rows * Ne * Ke, workload=f"64 experts, {rows} rows, {Ne}x{Ke}")
+    del Xe, We, qxe, qa, qwe, Ye
+    torch.cuda.empty_cache()
+    return out
+
+
+def _case_gemm(kind):
+    def setup(fp8, synth, dev):
+        if kind in ("fwd", "fwd_fused"):
+            wl = synth.mlp()
+            X, W = wl.tensors["X"].to(dev), wl.tensors["W"].to(dev)
+            qx, qw = fp8.quantize_group(X, "K"), fp8.quantize_block(W)
+            Y, qy = fp8.gemm(qx, qw, quantize_output=True)
+            if kind == "fwd":
+                return lambda: fp8.gemm(qx, qw, out=Y), 2.0 * M * N * K
+            return lambda: fp8.gemm(qx, qw, quantize_output=True, out=Y, out_q=qy), 2.0 * M * N * K
+        if kind in ("dgrad", "wgrad"):
+            wl = synth.backward()
+            dY, W, X = (wl.tensors[k].to(dev) for k in ("dY", "W", "X"))
+            if kind == "dgrad":
+                a, (_, b) = fp8.quantize_group(dY, "K"), fp8.quantize_block(W, True)
+            else:
+                a, b = fp8.quantize_group(dY, "M"), fp8.quantize_group(X, "M")
+            D = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=dev)
+            return lambda: fp8.gemm(a, b, kind, out=D), 2.0 * 8192 * 4096 * 4096
+        if kind == "mx":
+            wl = synth.mx()
+            a, b = fp8.quantize_mx(wl.tensors["X"].to(dev)), fp8.quantize_mx(wl.tensors["W"].to(dev))
+            D = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=dev)
+            return lambda: fp8.gemm(a, b, out=D), 2.0 * 2048 * 4096 * 4096
+        wl = synth.moe()
+        We = wl.tensors["W"]
+        G, Ne, Ke = We.shape
+        off = wl.tensors["offsets"].to(dev)
+        qa = fp8.permute_rows_mx(fp8.quantize_mx(wl.tensors["X"].to(dev)), wl.tensors["gather"].to(dev), off)
+        qw = fp8.quantize_mx(We.reshape(G * Ne, Ke).to(dev))
+        D = torch.empty((qa.rows, Ne), dtype=torch.bfloat16, device=dev)
+        return lambda: fp8.grouped_gemm(qa, qw, off, Ne, out=D), 2.0 * qa.rows * Ne * Ke
+    return setup
+
+
+def _case_quant(kind):
+    def setup(fp8, synth, dev):
+        if kind == "group_k":
+            X = synth.mlp().tensors["X"].to(dev)
+            q = fp8.quantize_group(X, "K")
+            return lambda: fp8.quantize_group(X, "K", out=q), None
+        if kind == "block":
+            W = synth.mlp().tensors["W"].to(dev)
+            q = fp8.quantize_block(W)
+            return lambda: fp8.quantize_block(W, out=q), None
+        if kind == "group_m":
+            X = synth.backward().tensors["X"].to(dev)
+            q = fp8.quantize_group(X, "M")
+            return lambda: fp8.quantize_group(X, "M", out=q), None
+        W = synth.mx().tensors["W"].to(dev)
+        q = fp8.quantize_mx(W)
+        return lambda: fp8.quantize_mx(W, out=q), None
+    return setup
+
+
+KERNEL_CASES = {
+    "gemm_blockwise_fwd": _case_gemm("fwd"), "gemm_blockwise_fwd_fused": _case_gemm("fwd_fused"),
+    "gemm_blockwise_dgrad": _case_gemm("dgrad"), "gemm_blockwise_wgrad": _case_gemm("wgrad"),
+    "gemm_mx_fwd": _case_gemm("mx"), "gemm_mx_grouped": _case_gemm("grouped"),
+    "quant_group_1x128": _case_quant("group_k"), "quant_block_128x128": _case_quant("block"),
+    "quant_group_128x1_T": _case_quant("group_m"), "quant_mx_1x32": _case_quant("mx"),
+}
+
+
+def run_single_kernel(args, fp8, synth, dev):
+    fn, flops = KERNEL_CASES[args.kernel](fp8, synth, dev)
+    flush = Flusher(dev)
+    ms = time_kernel(fn, flush, args.steps, warmup=args.warmup)
+    d = {"kernel": args.kernel, "ms": ms, "steps": args.steps, "warmup": args.warmup}
+    if flops:
+        d["TFLOP/s"] = flops / (ms * 1e-3) / 1e12
+    print(json.dumps(d), flush=True)
+
+
+def cpu_baseline_sample(X, W, rows_x, rows_w):
+    """The CPU oracle, as it stands, on rows_x rows of X and rows_w rows of W
+    (full K): quantize both, fp64 GEMM reference of that block, pack and
+    install the W slice.  Returns (seconds, flops, sample description)."""
+    import oracle
+    from block_scaled_fp8_e4m3_gb300 import synth
+    xs = synth.bf16_bits(X[:rows_x].contiguous())
+    ws = synth.bf16_bits(W[:rows_w].contiguous())
+    oracle.load()
+    t0 = time.perf_counter()
+    cx, sx = oracle.quant_group_1x128(xs)
+    cw, sw = oracle.quant_block_128x128(ws)
+    oracle.gemm_ref(oracle.dequant_group(cx, sx), oracle.dequant_block(cw, sw))
+    spec = [dict(tag=1, kind=oracle.KIND_FP8, recipe=oracle.RECIPE_BLOCKWISE, rows=rows_w, cols=K,
+                 layout=oracle.LAYOUT_BLOCK_128x128, data=cw, scales=sw)]
+    payload = oracle.sync_pack(spec)
+    dst = [dict(spec[0], data=np.zeros_like(cw), scales=np.zeros_like(sw))]
+    assert oracle.sync_install(payload, dst) == 0
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * rows_x * rows_w * K, (f"oracle on X[:{rows_x}] and W[:{rows_w}] (K=4096): quantize both, "
+                                           f"fp64 GEMM {rows_x}x{K}x{rows_w}, pack+install the W slice")
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    """CPU oracle arm: each step is a bounded sample of the workload."""
+    from block_scaled_fp8_e4m3_gb300 import synth
+    wl = synth.mlp()
+    X, W = wl.tensors["X"], wl.tensors["W"]
+    rx, rw = 128, 256
+    for _ in range(args.warmup):
+        cpu_baseline_sample(X, W, rx, rw)
+    tot, flops, desc = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        dt, fl, desc = cpu_baseline_sample(X, W, rx, rw)
+        tot += dt
+        flops += fl
+    value = flops / tot / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_per_step": desc, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-breakdown", action="store_true", help="skip the per-kernel table")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-reps", type=int, default=20)
+    ap.add_argument("--kernel", default=None, choices=sorted(KERNEL_CASES),
+                    help="run only this kernel on its workload (for profilers); prints its timing")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+
+    import block_scaled_fp8_e4m3_gb300 as fp8
+    from block_scaled_fp8_e4m3_gb300 import _build, synth
+    _build.build()
+    fp8.library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if args.kernel is not None:
+        run_single_kernel(args, fp8, synth, dev)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pk = peaks()
+
+    wl = synth.mlp()
+    Xh, Wh = wl.tensors["X"], wl.tensors["W"]
+    X, W = Xh.to(dev), Wh.to(dev)
+    step, payload_bytes, keep = make_step(fp8, X, W, dev)
+    flush = Flusher(dev)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+
+    phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] if os.environ.get(
+        "CUDA_VISIBLE_DEVICES") else str(local)
+    sampler = ClockSampler(int(phys) if phys.isdigit() else local)
+    time.sleep(0.2)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(args.steps):
+        flush()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        step(e)
+        evs.append(e)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+
+    per_kernel = np.zeros(5)
+    total_ms = 0.0
+    for e in evs:
+        seg = [e[i].elapsed_time(e[i + 1]) for i in range(5)]
+        per_kernel += seg
+        total_ms += e[0].elapsed_time(e[5])
+    per_kernel /= args.steps
+    ms_step = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    flops = 2.0 * M * N * K
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    # dominant kernel (the GEMM) against the FP8 dense peak
+    fp8_peak = 2.0 * pk["bf16_tflops"]
+    gemm_tf = flops / (per_kernel[2] * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "k_gemm_blockwise (fwd, fused 1x128 quant of Y)",
+                "achieved": round(gemm_tf, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                "frac": round(gemm_tf / fp8_peak, 4),
+                "peak_basis": f"2 x {pk['source']} bf16 burst {pk['bf16_tflops']} TFLOP/s (FP8:BF16 = 2:1)",
+                "traffic": None}
+    qx_gbs = M * K * (3 + 4 / 128) / (per_kernel[0] * 1e-3) / 1e9
+    qw_gbs = N * K * (3 + 4 / 16384) / (per_kernel[1] * 1e-3) / 1e9
+    step_kernels = {
+        "quant_group_1x128_X": {"ms": round(per_kernel[0], 5), "GB/s": round(qx_gbs, 1),
+                                "frac_hbm": round(qx_gbs / pk["hbm_gbs"], 4)},
+        "quant_block_128x128_W": {"ms": round(per_kernel[1], 5), "GB/s": round(qw_gbs, 1),
+                                  "frac_hbm": round(qw_gbs / pk["hbm_gbs"], 4)},
+        "gemm_blockwise_fwd_fused_quant": {"ms": round(per_kernel[2], 5), "TFLOP/s": round(gemm_tf, 1),
+                                           "frac_fp8_peak": round(gemm_tf / fp8_peak, 4)},
+        "sync_pack_W": {"ms": round(per_kernel[3], 5),
+                        "GB/s": round(2 * payload_bytes / (per_kernel[3] * 1e-3) / 1e9, 1)},
+        "sync_install_W": {"ms": round(per_kernel[4], 5),
+                           "GB/s": round(2 * payload_bytes / (per_kernel[4] * 1e-3) / 1e9, 1)},
+    }
+
+    # end to end through the public API with host buffers
+    Xp, Wp = Xh.pin_memory(), Wh.pin_memory()
+    Yp = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = min(args.steps, 20)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(e2e_steps):
+        X.copy_(Xp, non_blocking=True)
+        W.copy_(Wp, non_blocking=True)
+        Y = step()
+        Yp.copy_(Y, non_blocking=True)
+    t1.record()
+    torch.cuda.synchronize()
+    e2e_ms = t0.elapsed_time(t1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(Xh.numel() * 2 + Wh.numel() * 2), "d2h_bytes_per_step": int(M * N * 2),
+           "ms_per_step": e2e_ms, "steps": e2e_steps}
+
+    kernels = None
+    if not args.no_breakdown and rank == 0:
+        del keep
+        torch.cuda.empty_cache()
+        kernels = breakdown(fp8, synth, dev, flush, pk, args.kernel_reps)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, fl, desc = cpu_baseline_sample(Xh, Wh, 4096, 6144)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle", "sample": desc,
+               "seconds": round(dt, 2)}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "seed": 2,
+                           "step": "quant X 1x128, quant W 128x128, GEMM+fused quant of Y, sync pack W, install W",
+                           "l2": "flushed between steps (256 MB write)", "parallelism": f"replicas x{world}"},
+                "roofline": roofline, "step_kernels": step_kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clocks, "peaks": pk,
+                "kernels": kernels}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -143,19 +143,20 @@ def _bf16_2d(x: torch.Tensor) -> torch.Tensor:
 
 
 # ---------------------------------------------------------------- quantizers
-def quantize_group(x: torch.Tensor, axis: str = "K", stream=None) -> QTensor:
+def quantize_group(x: torch.Tensor, axis: str = "K", out: Optional[QTensor] = None, stream=None) -> QTensor:
     """1x128 groups along K (axis='K') or 128x1 groups along M written
-    transposed (axis='M', the WGrad operand layout)."""
+    transposed (axis='M', the WGrad operand layout).  `out` may supply
+    preallocated codes/scales."""
     x = _bf16_2d(x)
     M, K = x.shape
     dev = _dev(x)
     if axis == "K":
-        q = QTensor(torch.empty((M, K), dtype=torch.uint8, device=dev),
+        q = out or QTensor(torch.empty((M, K), dtype=torch.uint8, device=dev),
                     torch.empty((K // 128, M), dtype=torch.float32, device=dev), M, K, RECIPE_BLOCKWISE,
                     LAYOUT_GROUP_1x128)
         ax = AXIS_K
     elif axis == "M":
-        q = QTensor(torch.empty((K, M), dtype=torch.uint8, device=dev),
+        q = out or QTensor(torch.empty((K, M), dtype=torch.uint8, device=dev),
                     torch.empty((M // 128, K), dtype=torch.float32, device=dev), K, M, RECIPE_BLOCKWISE,
                     LAYOUT_GROUP_1x128)
         ax = AXIS_M
@@ -166,18 +167,19 @@ def quantize_group(x: torch.Tensor, axis: str = "K", stream=None) -> QTensor:
     return q
 
 
-def quantize_block(w: torch.Tensor, transposed: bool = False, stream=None):
+def quantize_block(w: torch.Tensor, transposed: bool = False, out: Optional[QTensor] = None,
+                   out_t: Optional[QTensor] = None, stream=None):
     """128x128 blocks; with transposed=True also returns the transposed copy
     (codes [K, N], scales [K/128, N/128]) used as the DGrad B operand."""
     w = _bf16_2d(w)
     N, K = w.shape
     dev = _dev(w)
-    q = QTensor(torch.empty((N, K), dtype=torch.uint8, device=dev),
+    q = out or QTensor(torch.empty((N, K), dtype=torch.uint8, device=dev),
                 torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev), N, K, RECIPE_BLOCKWISE,
                 LAYOUT_BLOCK_128x128)
     qt = None
     if transposed:
-        qt = QTensor(torch.empty((K, N), dtype=torch.uint8, device=dev),
+        qt = out_t or QTensor(torch.empty((K, N), dtype=torch.uint8, device=dev),
                      torch.empty((K // 128, N // 128), dtype=torch.float32, device=dev), K, N,
                      RECIPE_BLOCKWISE, LAYOUT_BLOCK_128x128)
     t = q.c()
@@ -187,12 +189,12 @@ def quantize_block(w: torch.Tensor, transposed: bool = False, stream=None):
     return (q, qt) if transposed else q
 
 
-def quantize_mx(x: torch.Tensor, stream=None) -> QTensor:
+def quantize_mx(x: torch.Tensor, out: Optional[QTensor] = None, stream=None) -> QTensor:
     """MXFP8: 1x32 blocks, E8M0 scales in the tensor-core atom layout."""
     x = _bf16_2d(x)
     R, K = x.shape
     dev = _dev(x)
-    q = QTensor(torch.empty((R, K), dtype=torch.uint8, device=dev),
+    q = out or QTensor(torch.empty((R, K), dtype=torch.uint8, device=dev),
                 torch.empty((mx_scale_bytes(R, K),), dtype=torch.uint8, device=dev), R, K, RECIPE_MX,
                 LAYOUT_MX_1x32)
     t = q.c()
@@ -200,7 +202,8 @@ def quantize_mx(x: torch.Tensor, stream=None) -> QTensor:
     return q
 
 
-def permute_rows_mx(q: QTensor, gather: torch.Tensor, offsets: torch.Tensor, stream=None) -> QTensor:
+def permute_rows_mx(q: QTensor, gather: torch.Tensor, offsets: torch.Tensor, out: Optional[QTensor] = None,
+                    stream=None) -> QTensor:
     """Gathers MX rows into expert-contiguous groups (dst row i = src row
     gather[i]); offsets int32 [G+1] on the device."""
     if gather.dtype != torch.int32 or offsets.dtype != torch.int32:
@@ -208,7 +211,7 @@ def permute_rows_mx(q: QTensor, gather: torch.Tensor, offsets: torch.Tensor, str
     total = gather.numel()
     G = offsets.numel() - 1
     dev = _dev(q.codes)
-    out = QTensor(torch.empty((total, q.cols), dtype=torch.uint8, device=dev),
+    out = out or QTensor(torch.empty((total, q.cols), dtype=torch.uint8, device=dev),
                   torch.empty((mx_grouped_scale_bytes(total, q.cols, G),), dtype=torch.uint8, device=dev),
                   total, q.cols, RECIPE_MX, LAYOUT_MX_1x32_GROUPED)
     src, dst = q.c(), out.c()
@@ -219,15 +222,15 @@ def permute_rows_mx(q: QTensor, gather: torch.Tensor, offsets: torch.Tensor, str
 
 # ---------------------------------------------------------------- GEMMs
 def gemm(A: QTensor, B: QTensor, op: str = "fwd", out_dtype=torch.bfloat16, quantize_output: bool = False,
-         out: Optional[torch.Tensor] = None, stream=None):
+         out: Optional[torch.Tensor] = None, out_q: Optional[QTensor] = None, stream=None):
     """D = A B^T with fp32 accumulation.  Returns D, or (D, QTensor of D)
     when quantize_output (1x128 for blockwise, 1x32 for MXFP8)."""
     M, N = A.rows, B.rows
     dev = _dev(A.codes)
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=dev)
-    dq = None
-    if quantize_output:
+    dq = out_q
+    if quantize_output and dq is None:
         if A.recipe == RECIPE_BLOCKWISE:
             dq = QTensor(torch.empty((M, N), dtype=torch.uint8, device=dev),
                          torch.empty((N // 128, M), dtype=torch.float32, device=dev), M, N, RECIPE_BLOCKWISE,
