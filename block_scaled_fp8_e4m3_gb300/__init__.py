@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "FP8Error", "QTensor", "SyncEntry", "library", "quantize_group", "quantize_block", "quantize_mx",
-    "permute_rows_mx", "gemm", "grouped_gemm", "sync_payload_size", "sync_pack", "sync_install",
+    "permute_rows_mx", "gemm", "grouped_gemm", "sync_payload_size", "sync_pack", "sync_install", "sync_install_noalloc",
     "status_poll", "mx_scale_bytes", "mx_grouped_scale_bytes",
     "RECIPE_BLOCKWISE", "RECIPE_MX", "LAYOUT_GROUP_1x128", "LAYOUT_BLOCK_128x128", "LAYOUT_MX_1x32",
     "LAYOUT_MX_1x32_GROUPED",
@@ -79,6 +79,7 @@ def library() -> C.CDLL:
         "fp8_sync_payload_size": [EP, I32, C.POINTER(C.c_uint64)],
         "fp8_sync_pack": [EP, I32, P, C.c_uint64, C.POINTER(C.c_uint64), S],
         "fp8_sync_install": [P, C.c_uint64, EP, I32, S],
+        "fp8_sync_install_noalloc": [P, C.c_uint64, EP, I32, S],
         "fp8_status_poll": [S],
     }
     for name, args in sigs.items():
@@ -310,6 +311,15 @@ def sync_install(payload: torch.Tensor, dst: Sequence[SyncEntry], stream=None, c
                                       _stream(stream)))
     if check:
         status_poll(stream)
+
+
+def sync_install_noalloc(payload: torch.Tensor, dst: Sequence[SyncEntry], stream=None):
+    """sync_install for callers that cannot allocate device memory: the
+    library's fixed scratch array is used instead (at most 128 entries;
+    concurrent calls race).  Blocks until the copy is done; a checksum
+    mismatch raises FP8Error(FP8_ERR_CHECKSUM)."""
+    _check(library().fp8_sync_install_noalloc(payload.data_ptr(), payload.numel(), _entries(dst), len(dst),
+                                              _stream(stream)))
 
 
 def status_poll(stream=None):

@@ -212,6 +212,108 @@ uint64_t table_checksum(const std::vector<uint8_t>& h) {
     return sum;
 }
 
+
+// ---------------------------------------------------------------- install without allocation
+// For callers that cannot allocate device memory: the checksum accumulator,
+// the verdict and the segment table of fp8_sync_install_noalloc live in this
+// file-scope device array instead of the per-device block the library would
+// otherwise cudaMalloc.  Every GPU that loads the library holds it until the
+// process exits.  All calls share it, so calls that overlap on the GPU race.
+constexpr int kNoAllocMaxEntries = 128;
+constexpr int kNoAllocMaxSegs = 2 * kNoAllocMaxEntries;
+constexpr uint64_t kNoAllocTableBytes = (kHeaderBytes + kEntryBytes * kNoAllocMaxEntries + 255) / 256 * 256;
+
+struct NoAllocScratch {
+    StatusBlock status;
+    CopySeg segs[kNoAllocMaxSegs];
+};
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[sizeof(NoAllocScratch)];
+
+std::mutex g_noalloc_mu;
+NoAllocScratch* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up once
+// per device; in host code the array's name is only a stand-in).
+NoAllocScratch* noalloc_scratch(fp8_status* err) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *err = cuda_fail(e, "cudaGetDevice");
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || ptr == nullptr) {
+            *err = cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+            return nullptr;
+        }
+        g_noalloc_ptr[dev] = static_cast<NoAllocScratch*>(ptr);
+    }
+    *err = FP8_OK;
+    return g_noalloc_ptr[dev];
+}
+
+// Scatter variant that reads its segment table and the verify kernel's
+// verdict from the scratch array; all segments in one launch.
+__global__ void __launch_bounds__(256) k_sync_scatter_table(const NoAllocScratch* sc, int nseg) {
+    if (*reinterpret_cast<const volatile unsigned int*>(&sc->status.verdict) != 0) return;
+    __shared__ uint64_t start[kNoAllocMaxSegs + 1];
+    if (threadIdx.x == 0) {
+        uint64_t acc = 0;
+        for (int i = 0; i < nseg; ++i) {
+            start[i] = acc;
+            acc += (sc->segs[i].bytes + 15) / 16;
+        }
+        start[nseg] = acc;
+    }
+    __syncthreads();
+    const uint64_t chunks = start[nseg];
+    for (uint64_t c = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; c < chunks;
+         c += (uint64_t)gridDim.x * blockDim.x) {
+        int lo = 0, hi = nseg;  // start[lo] <= c < start[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (start[mid] <= c) lo = mid; else hi = mid;
+        }
+        const CopySeg sg = sc->segs[lo];
+        const uint64_t off = (c - start[lo]) * 16;
+        const uint4 v = *reinterpret_cast<const uint4*>(sg.src + off);
+        if (off + 16 <= sg.bytes) {
+            *reinterpret_cast<uint4*>(sg.dst + off) = v;
+        } else {
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            for (uint64_t b = 0; off + b < sg.bytes; ++b) sg.dst[off + b] = (uint8_t)(w[b / 4] >> (8 * (b % 4)));
+        }
+    }
+}
+
+// Header + entry table into a caller-provided buffer (no allocation).
+void fill_table(uint8_t* h, uint64_t data_offset, const fp8_sync_entry* e, int32_t n, const EntryLayout* lay,
+                uint64_t total) {
+    memset(h, 0, (size_t)data_offset);
+    put64(&h[0], kSyncMagic);
+    put32(&h[8], 1);
+    put32(&h[12], (uint32_t)n);
+    put64(&h[16], total);
+    put64(&h[24], data_offset);
+    for (int32_t i = 0; i < n; ++i) {
+        uint8_t* t = &h[(size_t)(kHeaderBytes + kEntryBytes * (uint64_t)i)];
+        put64(t + 0, e[i].tag);
+        put32(t + 8, (uint32_t)e[i].kind);
+        put32(t + 12, (uint32_t)e[i].t.recipe);
+        put64(t + 16, (uint64_t)e[i].t.rows);
+        put64(t + 24, (uint64_t)e[i].t.cols);
+        put32(t + 32, (uint32_t)e[i].t.layout);
+        put64(t + 40, lay[i].data_off);
+        put64(t + 48, lay[i].data_bytes);
+        put64(t + 56, lay[i].scale_off);
+        put64(t + 64, lay[i].scale_bytes);
+    }
+}
+
 }  // namespace
 
 // ===========================================================================
@@ -562,6 +664,87 @@ fp8_status fp8_status_poll(fp8_stream_t stream) {
         return fail(FP8_ERR_TIMEOUT, "a bounded on-chip wait expired (site %u)", bits[1]);
     if (bits[0] & kErrChecksum) return fail(FP8_ERR_CHECKSUM, "sync payload checksum mismatch; nothing installed");
     return fail(FP8_ERR_INVALID_ARG, "a kernel rejected a device-side argument (e.g. a gather index)");
+}
+
+// Install for callers that cannot allocate device memory; see fp8bs.h.
+fp8_status fp8_sync_install_noalloc(const void* payload_dev, uint64_t bytes, const fp8_sync_entry* dst, int32_t n,
+                                    fp8_stream_t stream) {
+    if (n < 0 || (n > 0 && dst == nullptr)) return fail(FP8_ERR_INVALID_ARG, "bad entry list");
+    if (n > kNoAllocMaxEntries)
+        return fail(FP8_ERR_CAPACITY, "fp8_sync_install_noalloc takes at most %d entries (got %d); "
+                    "use fp8_sync_install", kNoAllocMaxEntries, n);
+    if (payload_dev == nullptr || (reinterpret_cast<uintptr_t>(payload_dev) & 255u))
+        return fail(FP8_ERR_ALIGNMENT, "payload must be a 256-byte aligned device pointer");
+    EntryLayout lay[kNoAllocMaxEntries];
+    uint64_t off = round_up(kHeaderBytes + kEntryBytes * (uint64_t)n, 256);
+    const uint64_t data_offset = off;
+    for (int32_t i = 0; i < n; ++i) {
+        uint64_t db, sb;
+        fp8_status s = entry_bytes(dst[i], i, &db, &sb);
+        if (s != FP8_OK) return s;
+        lay[i].data_off = off;
+        lay[i].data_bytes = db;
+        off = round_up(off + db, 256);
+        lay[i].scale_off = sb ? off : 0;
+        lay[i].scale_bytes = sb;
+        off = round_up(off + sb, 256);
+    }
+    const uint64_t total = off;
+    if (bytes < total)
+        return fail(FP8_ERR_BAD_PAYLOAD, "payload of %llu bytes, destinations need %llu", (unsigned long long)bytes,
+                    (unsigned long long)total);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const uint8_t* pay = static_cast<const uint8_t*>(payload_dev);
+
+    // header and table: read back and compare with what dst implies
+    uint8_t expect[kNoAllocTableBytes];
+    uint8_t got[kNoAllocTableBytes];
+    fill_table(expect, data_offset, dst, n, lay, total);
+    cudaError_t e = cudaMemcpyAsync(got, pay, (size_t)data_offset, cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) return cuda_fail(e, "sync_install_noalloc header read");
+    if (get64(&got[0]) != kSyncMagic || get32(&got[8]) != 1)
+        return fail(FP8_ERR_BAD_PAYLOAD, "not a version-1 FP8 sync payload");
+    if (get32(&got[12]) != (uint32_t)n)
+        return fail(FP8_ERR_BAD_PAYLOAD, "payload has %u entries, %d destinations", get32(&got[12]), n);
+    for (uint64_t i = 0; i < data_offset; ++i) {
+        if (i >= 32 && i < 40) continue;
+        if (got[i] != expect[i]) return fail(FP8_ERR_BAD_PAYLOAD, "payload header/table byte %llu differs",
+                                             (unsigned long long)i);
+    }
+    put64(&got[32], 0);
+    unsigned long long table_sum = 0;
+    for (uint64_t i = kHeaderBytes / 8; i < data_offset / 8; ++i) table_sum += host_mix64(get64(&got[8 * i]) ^ i);
+
+    fp8_status se;
+    NoAllocScratch* sc = noalloc_scratch(&se);
+    if (sc == nullptr) return se;
+    CopySeg segs[kNoAllocMaxSegs];
+    int nseg = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        segs[nseg++] = CopySeg{pay + lay[i].data_off, static_cast<uint8_t*>(dst[i].t.codes), lay[i].data_bytes, 0, 0};
+        if (lay[i].scale_bytes)
+            segs[nseg++] =
+                CopySeg{pay + lay[i].scale_off, static_cast<uint8_t*>(dst[i].t.scales), lay[i].scale_bytes, 0, 0};
+    }
+    // the previous call's contents stay in the array: clear the status part
+    e = cudaMemsetAsync(&sc->status, 0, sizeof(StatusBlock), cs);
+    if (e == cudaSuccess && nseg > 0)
+        e = cudaMemcpyAsync(sc->segs, segs, sizeof(CopySeg) * (size_t)nseg, cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "sync_install_noalloc set-up");
+    e = launch_sync_verify(pay, data_offset, total, table_sum, &sc->status, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "sync_install_noalloc verify");
+    if (nseg > 0) {
+        k_sync_scatter_table<<<152 * 4, 256, 0, cs>>>(sc, nseg);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "sync_install_noalloc scatter");
+    }
+    unsigned int verdict = 1;
+    e = cudaMemcpyAsync(&verdict, &sc->status.verdict, sizeof(verdict), cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) return cuda_fail(e, "sync_install_noalloc verdict read");
+    if (verdict != 0) return fail(FP8_ERR_CHECKSUM, "sync payload checksum mismatch; nothing installed");
+    return FP8_OK;
 }
 
 }  // extern "C"

@@ -261,6 +261,27 @@ fp8_status fp8_sync_pack(const fp8_sync_entry* entries, int32_t n, void* payload
 fp8_status fp8_sync_install(const void* payload_dev, uint64_t bytes, const fp8_sync_entry* dst,
                             int32_t n, fp8_stream_t stream);
 
+/* Install for callers that cannot allocate device memory.  The pages have
+ * no counterpart of this call; it exists for processes in which cudaMalloc
+ * is off limits while weights are swapped in -- for example a rollout engine
+ * whose memory pool has already claimed the device, or code running inside a
+ * region where allocation is forbidden.  fp8_sync_install itself allocates a
+ * small status block on first use; this variant allocates nothing.
+ * Result: the same bytes in the destinations as fp8_sync_install.
+ * Scratch: a fixed device array inside the library (about 10 KB, present on
+ * every GPU that loads the library until the process exits) holds the
+ * checksum accumulator, the verdict and the segment table, so at most 128
+ * entries per call; more returns FP8_ERR_CAPACITY.  The first call on a
+ * device looks up the array's device address; make that first call before
+ * any stream capture.  Every call shares the array and overwrites it: calls
+ * that overlap on the GPU (other streams, other host threads) race.
+ * Unlike fp8_sync_install it waits for the copy to finish and reports a
+ * checksum mismatch directly (FP8_ERR_CHECKSUM, nothing written); header or
+ * table mismatches return FP8_ERR_BAD_PAYLOAD before anything is enqueued.
+ * It allocates no device memory, and no host memory unless it fails. */
+fp8_status fp8_sync_install_noalloc(const void* payload_dev, uint64_t bytes, const fp8_sync_entry* dst,
+                                    int32_t n, fp8_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* Status and diagnostics                                                  */
 /* ---------------------------------------------------------------------- */
