@@ -48,11 +48,21 @@ constexpr int kEpiThreads = 256;
 constexpr int kMaxStages = 6;
 constexpr int kMaxGroups = 1024;
 
-// blockwise kernel
+// blockwise kernel: each ring stage holds K = 256 (two 128-wide scale blocks,
+// A and B as two 128-byte-wide swizzled halves each) so that the MMA thread
+// waits on one barrier per 8 MMAs (512 tensor-core cycles); the four TMEM
+// partial buffers of 128 columns are used as two pairs, one pair per stage.
 constexpr int kBwBN = 128;
-constexpr int kBwStages = 6;
-constexpr uint32_t kBwStageBytes = (BM + kBwBN) * BK;  // 32 KB
-constexpr uint32_t kBwTmemCols = 256;                   // two P buffers of 128 columns
+constexpr int kBwStages = 3;
+constexpr uint32_t kBwHalfBytes = 128 * BK;           // 16 KB: 128 rows x 128 bytes
+constexpr uint32_t kBwStageBytes = 4 * kBwHalfBytes;  // A0 A1 B0 B1 = 64 KB
+constexpr uint32_t kBwTmemCols = 512;
+constexpr int kBwEpiWarps = 8;                           // 2 per TMEM lane quarter
+constexpr int kBwLoaderWarp = kEpiWarp0 + kBwEpiWarps;     // fills the scale ring
+constexpr int kBwThreads = (kBwLoaderWarp + 1) * 32;
+constexpr int kBwSlices = kBwEpiWarps / 4;                // column slices of a row
+constexpr int kBwCols = kBwBN / kBwSlices;                // columns per epilogue thread
+constexpr int kBwChunks = kBwCols / 16;
 constexpr uint32_t kIdescBlockwise = idesc_f8f6f4(BM, kBwBN);
 
 // MX kernel
@@ -62,21 +72,33 @@ constexpr uint32_t kMxStageBytes = (BM + kMxBN) * BK;  // 48 KB
 constexpr uint32_t kSfStageBytes = 1536;                // SFA atom + two SFB atoms
 constexpr uint32_t kMxTmemCols = 512;                   // accumulator 256 + scale factors
 
-struct Barriers {
+struct alignas(16) Barriers {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
+    uint64_t acc_full[4];
+    uint64_t acc_empty[4];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
     int num_mtiles;  // MX: total 128-row tiles over all groups
-    float amax_xch[2][128];  // blockwise fused quantization: per-half row maxima
 };
 
-constexpr size_t kSmemBlockwise = 1024 + (size_t)kBwStages * kBwStageBytes + sizeof(Barriers);
+// blockwise kernel only (16-byte aligned: float4 reads and 16-byte cp.async)
+constexpr int kBwScaleSlots = 6;
+struct alignas(16) BwShared {
+    uint64_t sc_full[kBwScaleSlots];   // scale slot filled (32 cp.async arrivals of the loader warp)
+    uint64_t sc_empty[kBwScaleSlots];  // scale slot read by all epilogue warps
+    float amax_xch[kBwSlices][128];    // fused quantization: per-slice row maxima
+    float sa[kBwScaleSlots][2][128];   // per pair: row scales of the tile's 128 rows, 2 K blocks
+    float sb[kBwScaleSlots][2][128];   // per pair: column scales (WGrad) or the block scale at [.][k][0]
+};
+
+constexpr size_t kSmemBlockwise = 1024 + (size_t)kBwStages * kBwStageBytes + sizeof(Barriers) + sizeof(BwShared);
+static_assert(sizeof(Barriers) % 16 == 0, "BwShared must start 16-byte aligned");
+static_assert(kSmemBlockwise <= 232448, "blockwise shared memory over the 227 KB limit");
 constexpr size_t kSmemMx = 1024 + (size_t)kMxStages * (kMxStageBytes + kSfStageBytes) + sizeof(Barriers) +
                            2 * (kMaxGroups + 1) * sizeof(int);
+static_assert(kSmemMx <= 232448, "MX shared memory over the 227 KB limit");
 
 __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
     const uint32_t a = smem_u32(raw);
@@ -109,29 +131,6 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
                    "+r"(r[14]), "+r"(r[15])::"memory");
 }
 
-__device__ __forceinline__ void wait_chunk16(uint32_t (&r)[16]) {
-    tmem_ld_wait();
-    reg_fence16(r);
-}
-
-// acc[j] += P[j] * c for 16 columns
-__device__ __forceinline__ void promote16(float* acc, const uint32_t (&r)[16], float c) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = fmaf(__uint_as_float(r[i]), c, acc[i]);
-}
-
-// acc[j] += (P[j] * sb[j]) * sa for 16 columns with per-column scales sb
-__device__ __forceinline__ void promote16_cols(float* acc, const uint32_t (&r)[16], const float* sb, float sa) {
-    const float4* s4 = reinterpret_cast<const float4*>(sb);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 v = __ldg(s4 + i);
-        acc[4 * i + 0] = fmaf(__uint_as_float(r[4 * i + 0]) * v.x, sa, acc[4 * i + 0]);
-        acc[4 * i + 1] = fmaf(__uint_as_float(r[4 * i + 1]) * v.y, sa, acc[4 * i + 1]);
-        acc[4 * i + 2] = fmaf(__uint_as_float(r[4 * i + 2]) * v.z, sa, acc[4 * i + 2]);
-        acc[4 * i + 3] = fmaf(__uint_as_float(r[4 * i + 3]) * v.w, sa, acc[4 * i + 3]);
-    }
-}
 
 // MX 1x32 quantization of one row's 128 bf16 values: four blocks; returns
 // the four E8M0 bytes packed little-endian.
@@ -178,23 +177,80 @@ struct BwParams {
     int tiles_m, tiles_n;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Global pair index j of this CTA -> its tile and pair-within-tile.  Tiles
+// are visited blockIdx.x, blockIdx.x + gridDim.x, ...; every tile has
+// npairs = ceil(KB/2) pairs.
+struct PairCoord {
+    bool valid;
+    int tm, tn, p, nk;  // nk: K blocks in this pair (1 or 2)
+};
+
+__device__ __forceinline__ PairCoord bw_pair(int j, int npairs, int KB, int tiles_n, int num_tiles) {
+    PairCoord c;
+    const int i = j / npairs;
+    c.p = j - i * npairs;
+    const int tile = blockIdx.x + i * gridDim.x;
+    c.valid = tile < num_tiles;
+    c.tm = tile / tiles_n;
+    c.tn = tile - c.tm * tiles_n;
+    c.nk = KB - 2 * c.p >= 2 ? 2 : 1;
+    return c;
+}
+
+// acc[2i..2i+1] += (P * c) with packed fp32x2 FMAs, 16 columns
+__device__ __forceinline__ void promote16x2(float* acc, const uint32_t (&r)[16], float c) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        asm("{\n\t.reg .b64 a, x, y;\n\t"
+            "mov.b64 a, {%0, %1};\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %4};\n\t"
+            "fma.rn.f32x2 a, x, y, a;\n\tmov.b64 {%0, %1}, a;\n\t}\n"
+            : "+f"(acc[2 * i]), "+f"(acc[2 * i + 1])
+            : "f"(__uint_as_float(r[2 * i])), "f"(__uint_as_float(r[2 * i + 1])), "f"(c));
+}
+
+// acc += (P * sb) * sa with per-column sb (16 columns, sb from shared memory)
+__device__ __forceinline__ void promote16x2_cols(float* acc, const uint32_t (&r)[16], const float* sb, float sa) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 v = *reinterpret_cast<const float4*>(sb + 4 * i);
+        const float sv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            asm("{\n\t.reg .b64 a, x, s, t;\n\t"
+                "mov.b64 a, {%0, %1};\n\tmov.b64 x, {%2, %3};\n\tmov.b64 s, {%4, %5};\n\tmov.b64 t, {%6, %6};\n\t"
+                "mul.rn.f32x2 x, x, s;\n\tfma.rn.f32x2 a, x, t, a;\n\tmov.b64 {%0, %1}, a;\n\t}\n"
+                : "+f"(acc[4 * i + 2 * k]), "+f"(acc[4 * i + 2 * k + 1])
+                : "f"(__uint_as_float(r[4 * i + 2 * k])), "f"(__uint_as_float(r[4 * i + 2 * k + 1])),
+                  "f"(sv[2 * k]), "f"(sv[2 * k + 1]), "f"(sa));
+    }
+}
+
+__global__ void __launch_bounds__(kBwThreads, 1)
     k_gemm_blockwise(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const BwParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = aligned_smem(smem_raw);
     Barriers* bar = reinterpret_cast<Barriers*>(smem + kBwStages * kBwStageBytes);
+    BwShared* bws = reinterpret_cast<BwShared*>(bar + 1);
     volatile int* abort = &bar->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KB = p.K / BK;
+    const int npairs = (KB + 1) / 2;
+    const int num_tiles = p.tiles_m * p.tiles_n;
+    const int my_tiles = (int)blockIdx.x < num_tiles ? (num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total_pairs = my_tiles * npairs;
 
     if (threadIdx.x == 0) {
+        // full[s]: the producer's expect_tx arrival plus one arrival from each
+        // epilogue warp granting the TMEM pair (and, for WGrad, its scales)
         for (int s = 0; s < kBwStages; ++s) {
-            mbar_init(&bar->full[s], 1);
+            mbar_init(&bar->full[s], 1 + kBwEpiWarps);
             mbar_init(&bar->empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&bar->acc_full[b], 1);
-            mbar_init(&bar->acc_empty[b], kEpiThreads);
+        for (int b = 0; b < 4; ++b) mbar_init(&bar->acc_full[b], 1);  // [2*(pair&1) + half]
+        for (int i = 0; i < kBwScaleSlots; ++i) {
+            mbar_init(&bws->sc_full[i], 32);
+            mbar_init(&bws->sc_empty[i], kBwEpiWarps);
         }
         mbar_init(&bar->drain, 1);
         bar->abort = 0;
@@ -209,32 +265,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bar->tmem_base;
-    const int KB = p.K / BK;
-    const int num_tiles = p.tiles_m * p.tiles_n;
 
     if (warp == 0) {
         if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
-            uint32_t fills[kBwStages] = {0, 0, 0, 0, 0, 0};
+            uint32_t fills[kBwStages] = {0, 0, 0};
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                const int tm = tile / p.tiles_n, tn = tile % p.tiles_n;
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait_bounded(&bar->empty[s], ph ^ 1, abort, p.st, 1)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* stage = smem + s * kBwStageBytes;
-                    mbar_arrive_expect_tx(&bar->full[s], kBwStageBytes);
-                    tma_load_2d(stage, &tmA, &bar->full[s], kb * BK, tm * BM);
-                    tma_load_2d(stage + BM * BK, &tmB, &bar->full[s], kb * BK, tn * kBwBN);
-                    ++fills[s];
-                    if (++s == kBwStages) {
-                        s = 0;
-                        ph ^= 1;
-                    }
+            for (int j = 0; j < total_pairs && ok; ++j) {
+                const PairCoord c = bw_pair(j, npairs, KB, p.tiles_n, num_tiles);
+                const int s = j % kBwStages;
+                if (!mbar_wait_bounded(&bar->empty[s], ((j / kBwStages) & 1) ^ 1, abort, p.st, 1)) {
+                    ok = false;
+                    break;
                 }
+                uint8_t* stage = smem + s * kBwStageBytes;
+                mbar_arrive_expect_tx(&bar->full[s], (uint32_t)c.nk * 2 * kBwHalfBytes);
+                const int k0 = 2 * c.p * BK;
+                tma_load_2d(stage, &tmA, &bar->full[s], k0, c.tm * BM);
+                tma_load_2d(stage + 2 * kBwHalfBytes, &tmB, &bar->full[s], k0, c.tn * kBwBN);
+                if (c.nk == 2) {
+                    tma_load_2d(stage + kBwHalfBytes, &tmA, &bar->full[s], k0 + BK, c.tm * BM);
+                    tma_load_2d(stage + 3 * kBwHalfBytes, &tmB, &bar->full[s], k0 + BK, c.tn * kBwBN);
+                }
+                ++fills[s];
             }
             if (!ok)
                 for (int i = 0; i < kBwStages; ++i)
@@ -242,139 +294,228 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            int s = 0, ab = 0;
-            uint32_t ph = 0, aph = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait_bounded(&bar->acc_empty[ab], aph ^ 1, abort, p.st, 2) ||
-                        !mbar_wait_bounded(&bar->full[s], ph, abort, p.st, 3)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_addr = smem_u32(smem + s * kBwStageBytes);
-                    const uint64_t adesc = sdesc_k_sw128(a_addr);
-                    const uint64_t bdesc = sdesc_k_sw128(a_addr + BM * BK);
-                    const uint32_t d = tmem + (uint32_t)(ab * kBwBN);
+            for (int j = 0; j < total_pairs; ++j) {
+                const PairCoord c = bw_pair(j, npairs, KB, p.tiles_n, num_tiles);
+                const int s = j % kBwStages;
+                if (!mbar_wait_bounded(&bar->full[s], (j / kBwStages) & 1, abort, p.st, 3)) break;
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(smem + s * kBwStageBytes);
+                const uint32_t pbuf = tmem + (uint32_t)((j & 1) * 2 * kBwBN);
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k)
-                        tc_mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, kIdescBlockwise, k > 0 ? 1u : 0u);
-                    tc_commit(&bar->empty[s]);
-                    tc_commit(&bar->acc_full[ab]);
-                    if (++s == kBwStages) {
-                        s = 0;
-                        ph ^= 1;
+                for (int hk = 0; hk < 2; ++hk) {
+                    if (hk < c.nk) {
+                        const uint64_t adesc = sdesc_k_sw128(a_addr + hk * kBwHalfBytes);
+                        const uint64_t bdesc = sdesc_k_sw128(a_addr + (2 + hk) * kBwHalfBytes);
+#pragma unroll
+                        for (int k = 0; k < BK / 32; ++k)
+                            tc_mma_f8f6f4(pbuf + (uint32_t)(hk * kBwBN), adesc + 2 * k, bdesc + 2 * k, kIdescBlockwise,
+                                          k > 0 ? 1u : 0u);
                     }
-                    ab ^= 1;
-                    if (ab == 0) aph ^= 1;
+                    if (hk == 1) tc_commit(&bar->empty[s]);
+                    // each half is handed to the epilogue as soon as it is done
+                    // (a half-pair at an odd-K tail still commits, keeping phases aligned)
+                    tc_commit(&bar->acc_full[2 * (j & 1) + hk]);
                 }
             }
             tc_commit(&bar->drain);
             mbar_wait_drain(&bar->drain, 0, p.st);
         }
+    } else if (warp == kBwLoaderWarp) {
+        // scale loader: per pair, the row scales of the tile's 128 rows and
+        // the column (WGrad) or block scales of its two K blocks, by cp.async
+        // into ring slot j%6; each lane's copies complete onto sc_full.
+        int ti = 0, pp = 0, tm = 0, tn = 0;
+        for (int j = 0; j < total_pairs; ++j) {
+            if (pp == 0) {
+                const int tile = blockIdx.x + ti * gridDim.x;
+                tm = tile / p.tiles_n;
+                tn = tile - tm * p.tiles_n;
+            }
+            const int slot = j % kBwScaleSlots;
+            if (!mbar_wait_bounded(&bws->sc_empty[slot], ((j / kBwScaleSlots) & 1) ^ 1, abort, p.st, 7)) break;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int kb = 2 * pp + k;
+                const bool kok = kb < KB;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int m = tm * BM + 4 * lane + i;
+                    const bool ok = kok && m < p.M;
+                    const float* src = ok ? p.sa + (size_t)kb * p.M + m : p.sa;
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                                     smem_u32(&bws->sa[slot][k][4 * lane + i])),
+                                 "l"(src), "r"(ok ? 4 : 0)
+                                 : "memory");
+                }
+                if (!p.sb_per_row) {
+                    if (lane == 0) {
+                        const float* src = kok ? p.sb + (size_t)tn * KB + kb : p.sb;
+                        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(&bws->sb[slot][k][0])),
+                                     "l"(src), "r"(kok ? 4 : 0)
+                                     : "memory");
+                    }
+                } else {
+                    const float* src = kok ? p.sb + (size_t)kb * p.N + tn * kBwBN + 4 * lane : p.sb;
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                                     smem_u32(&bws->sb[slot][k][4 * lane])),
+                                 "l"(src), "r"(kok ? 16 : 0)
+                                 : "memory");
+                }
+            }
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&bws->sc_full[slot]))
+                         : "memory");
+            if (++pp == npairs) {
+                pp = 0;
+                ++ti;
+            }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
     } else {
-        // epilogue: warp (q = warp%4, h) promotes rows 32q.. , columns 64h..64h+63
+        // epilogue: warp (q = warp%4, h) promotes rows 32q.. , columns kBwCols*h ..
         const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
+        const int ew = warp - kEpiWarp0;
         const int rl = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        int ab = 0;
-        uint32_t aph = 0;
+        (void)ew;
+        // grant the TMEM pairs of pairs 0 and 1
+        if (lane == 0) {
+            mbar_arrive(&bar->full[0]);
+            mbar_arrive(&bar->full[1]);
+        }
+
         bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            const int tm = tile / p.tiles_n, tn = tile % p.tiles_n;
-            const int m = tm * BM + rl;
-            const int ncol0 = tn * kBwBN + 64 * h;
-            const bool mvalid = m < p.M;
-            float acc[64];
+        for (int ti = 0; ti < my_tiles && ok; ++ti) {
+        const int tile = blockIdx.x + ti * gridDim.x;
+        const int ctm = tile / p.tiles_n, ctn = tile - ctm * p.tiles_n;
+        float acc[kBwCols];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
-            float sa_next = mvalid ? __ldg(p.sa + m) : 0.0f;
-            for (int kb = 0; kb < KB; ++kb) {
-                const float sa_v = sa_next;
-                if (kb + 1 < KB) sa_next = mvalid ? __ldg(p.sa + (size_t)(kb + 1) * p.M + m) : 0.0f;
-                float cs = 0.0f;
-                if (!p.sb_per_row) cs = sa_v * __ldg(p.sb + (size_t)tn * KB + kb);
-                if (!mbar_wait_bounded(&bar->acc_full[ab], aph, abort, p.st, 4)) {
+        for (int i = 0; i < kBwCols; ++i) acc[i] = 0.0f;
+        for (int pp = 0; pp < npairs; ++pp) {
+            const int j = ti * npairs + pp;
+            PairCoord c;
+            c.p = pp;
+            c.nk = KB - 2 * pp >= 2 ? 2 : 1;
+            const int slot = j % kBwScaleSlots;
+            if (!mbar_wait_bounded(&bws->sc_full[slot], (j / kBwScaleSlots) & 1, abort, p.st, 5) ||
+                !mbar_wait_bounded(&bar->acc_full[2 * (j & 1)], (j >> 1) & 1, abort, p.st, 4)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tb = tmem + lane_base + (uint32_t)((j & 1) * 2 * kBwBN + kBwCols * h);
+            uint32_t r[kBwChunks][16];
+#pragma unroll
+            for (int cc = 0; cc < kBwChunks; ++cc) tmem_ld_32x32b_x16(tb + 16 * cc, r[cc]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int cc = 0; cc < kBwChunks; ++cc) reg_fence16(r[cc]);
+            const float sa0 = bws->sa[slot][0][rl], sa1 = bws->sa[slot][1][rl];
+            const float* sbs0 = &bws->sb[slot][0][kBwCols * h];
+            const float* sbs1 = &bws->sb[slot][1][kBwCols * h];
+            if (!p.sb_per_row) {
+                const float cs = sa0 * bws->sb[slot][0][0];
+#pragma unroll
+                for (int cc = 0; cc < kBwChunks; ++cc) promote16x2(acc + 16 * cc, r[cc], cs);
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < kBwChunks; ++cc) promote16x2_cols(acc + 16 * cc, r[cc], sbs0 + 16 * cc, sa0);
+            }
+            if (c.nk == 2) {
+                if (!mbar_wait_bounded(&bar->acc_full[2 * (j & 1) + 1], (j >> 1) & 1, abort, p.st, 6)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tb = tmem + lane_base + (uint32_t)(ab * kBwBN + 64 * h);
-                // 4 chunks of 16 columns, double-buffered: chunk c+1 is in
-                // flight while chunk c is promoted
-                uint32_t r[2][16];
-                tmem_ld_32x32b_x16(tb, r[0]);
-                wait_chunk16(r[0]);
-                if (!p.sb_per_row) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c < 3) tmem_ld_32x32b_x16(tb + 16 * (c + 1), r[(c + 1) & 1]);
-                        promote16(acc + 16 * c, r[c & 1], cs);
-                        if (c < 3) wait_chunk16(r[(c + 1) & 1]);
-                    }
-                } else {
-                    const float* sbs = p.sb + (size_t)kb * p.N + ncol0;  // per-column scales of B (WGrad)
+                for (int cc = 0; cc < kBwChunks; ++cc) tmem_ld_32x32b_x16(tb + kBwBN + 16 * cc, r[cc]);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c < 3) tmem_ld_32x32b_x16(tb + 16 * (c + 1), r[(c + 1) & 1]);
-                        promote16_cols(acc + 16 * c, r[c & 1], sbs + 16 * c, sa_v);
-                        if (c < 3) wait_chunk16(r[(c + 1) & 1]);
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(&bar->acc_empty[ab]);
-                ab ^= 1;
-                if (ab == 0) aph ^= 1;
+                for (int cc = 0; cc < kBwChunks; ++cc) reg_fence16(r[cc]);
             }
-            if (!ok) break;
+            // the pair's TMEM is read: grant it to pair j+2 (whose stage is j+2)
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && j + 2 < total_pairs) mbar_arrive(&bar->full[(j + 2) % kBwStages]);
+            if (c.nk == 2) {
+                if (!p.sb_per_row) {
+                    const float cs = sa1 * bws->sb[slot][1][0];
+#pragma unroll
+                    for (int cc = 0; cc < kBwChunks; ++cc) promote16x2(acc + 16 * cc, r[cc], cs);
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < kBwChunks; ++cc)
+                        promote16x2_cols(acc + 16 * cc, r[cc], sbs1 + 16 * cc, sa1);
+                }
+            }
+            // the scale slot is read: hand it back to the loader warp
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bws->sc_empty[slot]);
+        }
+        if (!ok) break;
+        {
+            // tile done: store D (and the fused 1x128 quantization)
+            const int m = ctm * BM + rl;
+            const int ncol0 = ctn * kBwBN + kBwCols * h;
+            const bool mvalid = m < p.M;
             if (p.d_f32) {
                 if (mvalid) {
-                    float* d = reinterpret_cast<float*>(p.D) + (size_t)m * p.ldd + ncol0;
+                    float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.D) + (size_t)m * p.ldd + ncol0);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        reinterpret_cast<float4*>(d)[i] =
-                            make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                    for (int i = 0; i < kBwCols / 4; ++i)
+                        d[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
                 }
-                continue;
-            }
-            uint32_t packed[32];
+            } else {
+                uint32_t packed[kBwCols / 2];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) packed[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
-            if (mvalid) {
-                uint4* d = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.D) + (size_t)m * p.ldd + ncol0);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-            }
-            if (p.q_codes != nullptr) {
-                // 1x128 group = this thread's 64 columns + the partner warp's 64:
-                // exchange the half-row maxima through shared memory
-                float a = 0.0f;
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    a = fmaxf(a, fmaxf(fabsf(bf16_lo(packed[j])), fabsf(bf16_hi(packed[j]))));
-                bar->amax_xch[h][rl] = a;
-                asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
-                a = fmaxf(a, bar->amax_xch[h ^ 1][rl]);
-                asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
-                const float sc = group_scale(a);
+                for (int i = 0; i < kBwCols / 2; ++i) packed[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
                 if (mvalid) {
-                    uint8_t* codes = p.q_codes + (size_t)m * p.N + ncol0;
+                    uint4* d =
+                        reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.D) + (size_t)m * p.ldd + ncol0);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t w[4];
+                    for (int i = 0; i < kBwCols / 8; ++i)
+                        d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                }
+                if (p.q_codes != nullptr) {
+                    // a 1x128 group spans the kBwSlices warps of this lane
+                    // quarter: exchange the slice maxima through shared memory
+                    float a = 0.0f;
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint32_t p0 = packed[8 * i + 2 * k], p1 = packed[8 * i + 2 * k + 1];
-                            w[k] = e4m3x2(__fdiv_rn(bf16_lo(p0), sc), __fdiv_rn(bf16_hi(p0), sc)) |
-                                   (e4m3x2(__fdiv_rn(bf16_lo(p1), sc), __fdiv_rn(bf16_hi(p1), sc)) << 16);
+                    for (int i = 0; i < kBwCols / 2; ++i)
+                        a = fmaxf(a, fmaxf(fabsf(bf16_lo(packed[i])), fabsf(bf16_hi(packed[i]))));
+                    bws->amax_xch[h][rl] = a;
+                    asm volatile("bar.sync %0, %1;" ::"r"(1 + q), "r"(32 * kBwSlices) : "memory");
+#pragma unroll
+                    for (int o = 0; o < kBwSlices; ++o) a = fmaxf(a, bws->amax_xch[o][rl]);
+                    asm volatile("bar.sync %0, %1;" ::"r"(1 + q), "r"(32 * kBwSlices) : "memory");
+                    const float sc = group_scale(a);
+                    if (mvalid) {
+                        uint8_t* codes = p.q_codes + (size_t)m * p.N + ncol0;
+#pragma unroll
+                        for (int i = 0; i < kBwCols / 16; ++i) {
+                            float f0[8], f1[8];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                f0[2 * k] = bf16_lo(packed[8 * i + k]);
+                                f0[2 * k + 1] = bf16_hi(packed[8 * i + k]);
+                                f1[2 * k] = bf16_lo(packed[8 * i + 4 + k]);
+                                f1[2 * k + 1] = bf16_hi(packed[8 * i + 4 + k]);
+                            }
+                            uint4 w;
+                            w.x = e4m3x2(__fdiv_rn(f0[0], sc), __fdiv_rn(f0[1], sc)) |
+                                  (e4m3x2(__fdiv_rn(f0[2], sc), __fdiv_rn(f0[3], sc)) << 16);
+                            w.y = e4m3x2(__fdiv_rn(f0[4], sc), __fdiv_rn(f0[5], sc)) |
+                                  (e4m3x2(__fdiv_rn(f0[6], sc), __fdiv_rn(f0[7], sc)) << 16);
+                            w.z = e4m3x2(__fdiv_rn(f1[0], sc), __fdiv_rn(f1[1], sc)) |
+                                  (e4m3x2(__fdiv_rn(f1[2], sc), __fdiv_rn(f1[3], sc)) << 16);
+                            w.w = e4m3x2(__fdiv_rn(f1[4], sc), __fdiv_rn(f1[5], sc)) |
+                                  (e4m3x2(__fdiv_rn(f1[6], sc), __fdiv_rn(f1[7], sc)) << 16);
+                            reinterpret_cast<uint4*>(codes)[i] = w;
                         }
-                        reinterpret_cast<uint4*>(codes)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                        if (h == 0) p.q_scales[(size_t)ctn * p.M + m] = sc;
                     }
-                    if (h == 0) p.q_scales[(size_t)tn * p.M + m] = sc;
                 }
             }
+        }
         }
     }
 
@@ -443,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar->empty[s], 1);
         }
         mbar_init(&bar->acc_full[0], 1);
-        mbar_init(&bar->acc_empty[0], kEpiThreads);
+        mbar_init(&bar->acc_empty[0], kEpiThreads / 32);
         mbar_init(&bar->drain, 1);
         bar->abort = 0;
         fence_mbar_init();
@@ -596,7 +737,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bar->acc_empty[0]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->acc_empty[0]);
             aph ^= 1;
             const int64_t m = (int64_t)c.row0 + rl;
             if (mvalid && hvalid) {
@@ -689,7 +831,7 @@ cudaError_t launch_gemm_blockwise(const GemmBlockwiseArgs& a, StatusBlock* statu
     cudaError_t e = cudaFuncSetAttribute(k_gemm_blockwise, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBlockwise);
     if (e != cudaSuccess) return e;
-    k_gemm_blockwise<<<grid, kThreads, kSmemBlockwise, st>>>(tmA, tmB, p);
+    k_gemm_blockwise<<<grid, kBwThreads, kSmemBlockwise, st>>>(tmA, tmB, p);
     return cudaGetLastError();
 }
 

@@ -40,7 +40,7 @@ __device__ __forceinline__ float amax8(const float (&f)[8]) {
     return a;
 }
 
-// 8 values divided by s (IEEE) and encoded; returns 8 codes as two words.
+// 8 values divided by s (IEEE fp32 division) and encoded: 8 codes in two words.
 __device__ __forceinline__ uint2 encode8_div(const float (&f)[8], float s) {
     uint2 r;
     r.x = e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) | (e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
@@ -155,9 +155,10 @@ __global__ void __launch_bounds__(256) k_quant_group_m(const uint16_t* __restric
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const float s = col_scale[chunk * 8 + j];
-        const uint32_t lo = e4m3x2(__fdiv_rn(f[0][j], s), __fdiv_rn(f[1][j], s));
-        const uint32_t hi = e4m3x2(__fdiv_rn(f[2][j], s), __fdiv_rn(f[3][j], s));
-        tile[(chunk * 8 + j) * 33 + quad] = lo | (hi << 16);
+        float q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = __fdiv_rn(f[i][j], s);
+        tile[(chunk * 8 + j) * 33 + quad] = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
     }
     __syncthreads();
 #pragma unroll
