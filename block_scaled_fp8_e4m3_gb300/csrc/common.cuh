@@ -63,48 +63,6 @@ __device__ __forceinline__ float group_scale(float amax) {
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
-// Fast path for the E4M3 code of the IEEE quotient x/s.  y = RN(x * RN(1/s))
-// differs from RN(x/s) by at most 3 fp32 ulps (two roundings of 2^-24
-// relative error each, against one of 2^-24).  Both round to the same E4M3
-// code unless an E4M3 rounding midpoint lies between them; in the normal E4M3
-// range every midpoint has its 20 fp32 mantissa bits below the 3 kept ones
-// equal to 0x80000, and powers of two (where the ulp changes) are E4M3
-// values, not midpoints.  So when y's low 20 bits are not within [-4, +3]
-// ulps of 0x80000 (a window covering the 3-ulp bound on both sides)
-// (and |y| >= 2^-5, above the E4M3 subnormal range) its code is the code of
-// RN(x/s); otherwise the caller takes the IEEE division.  Every true quotient
-// has |x/s| <= 448(1+2^-23), so |y| > 512 (or a non-finite y) only happens
-// when 1/s overflowed for a group of tiny values: exact path as well.
-__device__ __forceinline__ bool e4m3_needs_exact(float y) {
-    const uint32_t a = __float_as_uint(y) & 0x7FFFFFFFu;
-    // y = +-0 only when x is +-0 or x/s is far below the E4M3 range: both
-    // encode to a signed zero, so zero stays on the fast path
-    return a != 0u &&
-           ((a - 0x3D000000u) > (0x44000000u - 0x3D000000u) || ((a + 4u) & 0xFFFF8u) == 0x80000u);
-}
-
-// Eight quotients x/s as E4M3 codes (two words), exactly as by IEEE division.
-__device__ __forceinline__ uint2 encode8_quot(const float (&f)[8], float s, float r) {
-    float q[8];
-    bool exact = false;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        q[i] = __fmul_rn(f[i], r);
-        exact |= e4m3_needs_exact(q[i]);
-    }
-    // branch uniform over the active lanes: the divisions are skipped, not
-    // predicated off, unless some lane needs them
-    if (__any_sync(__activemask(), exact)) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (e4m3_needs_exact(q[i])) q[i] = __fdiv_rn(f[i], s);
-    }
-    uint2 c;
-    c.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
-    c.y = e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16);
-    return c;
-}
-
 // MX shared exponent e = clamp(floor(log2 amax) - 8, -127, 127) from the fp32
 // bit fields (no log2 evaluation); -127 for an all-zero block.
 __device__ __forceinline__ int mx_exponent(float amax) {
