@@ -163,6 +163,13 @@ __device__ __forceinline__ uint32_t quant_row_mx(const uint32_t (&packed)[64], u
 // ===========================================================================
 // Blockwise (fp32-scale) GEMM with promotion
 // ===========================================================================
+// 32-byte global store (one full L2 sector per lane).
+__device__ __forceinline__ void st_v8(void* ptr, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 struct BwParams {
     const float* sa;
     const float* sb;
@@ -175,6 +182,7 @@ struct BwParams {
     float* q_scales;
     StatusBlock* st;
     int tiles_m, tiles_n;
+    int d_v8, q_v8;  // D rows / code rows allow 32-byte stores
 };
 
 // Global pair index j of this CTA -> its tile and pair-within-tile.  Tiles
@@ -459,21 +467,37 @@ __global__ void __launch_bounds__(kBwThreads, 1)
             const bool mvalid = m < p.M;
             if (p.d_f32) {
                 if (mvalid) {
-                    float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.D) + (size_t)m * p.ldd + ncol0);
+                    float* drow = reinterpret_cast<float*>(p.D) + (size_t)m * p.ldd + ncol0;
+                    if (p.d_v8) {
 #pragma unroll
-                    for (int i = 0; i < kBwCols / 4; ++i)
-                        d[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                        for (int i = 0; i < kBwCols / 8; ++i) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(acc[8 * i + k]);
+                            st_v8(drow + 8 * i, w);
+                        }
+                    } else {
+                        float4* d = reinterpret_cast<float4*>(drow);
+#pragma unroll
+                        for (int i = 0; i < kBwCols / 4; ++i)
+                            d[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                    }
                 }
             } else {
                 uint32_t packed[kBwCols / 2];
 #pragma unroll
                 for (int i = 0; i < kBwCols / 2; ++i) packed[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
                 if (mvalid) {
-                    uint4* d =
-                        reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.D) + (size_t)m * p.ldd + ncol0);
+                    uint16_t* drow = reinterpret_cast<uint16_t*>(p.D) + (size_t)m * p.ldd + ncol0;
+                    if (p.d_v8) {
 #pragma unroll
-                    for (int i = 0; i < kBwCols / 8; ++i)
-                        d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                        for (int i = 0; i < kBwCols / 16; ++i) st_v8(drow + 16 * i, packed + 8 * i);
+                    } else {
+                        uint4* d = reinterpret_cast<uint4*>(drow);
+#pragma unroll
+                        for (int i = 0; i < kBwCols / 8; ++i)
+                            d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                    }
                 }
                 if (p.q_codes != nullptr) {
                     // a 1x128 group spans the kBwSlices warps of this lane
@@ -490,6 +514,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                     const float sc = group_scale(a);
                     if (mvalid) {
                         uint8_t* codes = p.q_codes + (size_t)m * p.N + ncol0;
+                        uint32_t cw[kBwCols / 4];
 #pragma unroll
                         for (int i = 0; i < kBwCols / 16; ++i) {
                             float f0[8], f1[8];
@@ -509,7 +534,19 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                                   (e4m3x2(__fdiv_rn(f1[2], sc), __fdiv_rn(f1[3], sc)) << 16);
                             w.w = e4m3x2(__fdiv_rn(f1[4], sc), __fdiv_rn(f1[5], sc)) |
                                   (e4m3x2(__fdiv_rn(f1[6], sc), __fdiv_rn(f1[7], sc)) << 16);
-                            reinterpret_cast<uint4*>(codes)[i] = w;
+                            cw[4 * i] = w.x;
+                            cw[4 * i + 1] = w.y;
+                            cw[4 * i + 2] = w.z;
+                            cw[4 * i + 3] = w.w;
+                        }
+                        if (p.q_v8) {
+#pragma unroll
+                            for (int i = 0; i < kBwCols / 32; ++i) st_v8(codes + 32 * i, cw + 8 * i);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < kBwCols / 16; ++i)
+                                reinterpret_cast<uint4*>(codes)[i] =
+                                    make_uint4(cw[4 * i], cw[4 * i + 1], cw[4 * i + 2], cw[4 * i + 3]);
                         }
                         if (h == 0) p.q_scales[(size_t)ctn * p.M + m] = sc;
                     }
@@ -826,6 +863,9 @@ cudaError_t launch_gemm_blockwise(const GemmBlockwiseArgs& a, StatusBlock* statu
     p.st = status;
     p.tiles_m = (int)((a.M + BM - 1) / BM);
     p.tiles_n = (int)((a.N + kBwBN - 1) / kBwBN);
+    const int64_t row_bytes = a.ldd * (a.d_f32 ? 4 : 2);
+    p.d_v8 = (reinterpret_cast<uintptr_t>(a.D) % 32 == 0) && (row_bytes % 32 == 0);
+    p.q_v8 = reinterpret_cast<uintptr_t>(a.q_codes) % 32 == 0;
     const int tiles = p.tiles_m * p.tiles_n;
     const int grid = tiles < sm_count() ? tiles : sm_count();
     cudaError_t e = cudaFuncSetAttribute(k_gemm_blockwise, cudaFuncAttributeMaxDynamicSharedMemorySize,
