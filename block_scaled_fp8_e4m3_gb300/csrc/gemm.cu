@@ -1,17 +1,14 @@
 // gemm.cu -- block-scaled FP8 GEMMs on the 5th-generation tensor cores.
 //
-// Both kernels compute D = A B^T with A [M][K], B [N][K] E4M3 codes (K-major)
-// and are persistent, warp-specialised, one CTA per SM, 10 warps:
+// Both kernels compute D = A B^T with A [M][K], B [N][K] E4M3 codes (K-major),
+// are persistent and warp-specialised, and run one CTA per SM:
 //   warp 0      TMA producer: A and B tiles (+ the MX scale atoms) per
 //               128-wide K block into a multi-stage shared-memory ring
-//   warp 1      allocates TMEM; one thread issues tcgen05.mma (M=128, K=32,
-//               four per K block) and tcgen05.commit
-//   warps 2-9   epilogue: tcgen05.ld of the fp32 accumulator; warp w owns TMEM
-//               lanes 32*(w%4).. and half of the tile's columns, so each lane
-//               quarter is served by two warps.
-// Ten warps put three warps on two of the four SM sub-partitions, whose
-// 16K-register files then allow at most 168 registers per thread; the tile
-// shapes below are chosen so that the epilogue fits without spilling.
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma (K=32, four per
+//               K block and N slice) and tcgen05.commit
+//   warps 2..   epilogue: tcgen05.ld of the fp32 partials / accumulator; warp w
+//               may only touch TMEM lanes 32*(w%4).., so each lane quarter is
+//               served by (number of epilogue warps) / 4 warps.
 //
 // Blockwise recipe (fp32 scales; "Jet-RL: Enabling On-Policy FP8 ...",
 // "Kwantisatieschema"): the fp32 scales cannot be applied inside the MMA, so
@@ -19,19 +16,21 @@
 // the epilogue warps promote it into register accumulators:
 //   acc[m][n] += P[m][n] * sa[kb][m] * sb(n, kb)
 // with sb per 128x128 weight block (forward, DGrad) or per row of B (WGrad,
-// whose operands come from 128x1 groups).  Tile 128x128 (64 accumulators per
-// epilogue thread); P double-buffered (2 x 128 TMEM columns) so the tensor
-// core fills one while the other is promoted; 6-stage ring.
+// whose operands come from 128x1 groups).  CTA pairs (clusters of two, 2-SM
+// tcgen05.mma.cta_group::2, M=256) compute 256x256 tiles; 16 epilogue warps
+// per CTA hold a 128x256 fp32 result (64 accumulators per thread); a scale
+// loader warp stages sa/sb through shared memory.
 //
 // MXFP8 recipe ("Anyscale、SkyRL で FP8 ...", "Deep dive: FP8 quantization
 // with FP32 and power-of-two block scales": Blackwell tensor cores apply
 // power-of-two block scales themselves): kind::mxf8f6f4.block_scale with the
 // E8M0 scale atoms copied shared -> TMEM by tcgen05.cp; the accumulator stays
-// in TMEM for the whole K loop.  Tile 128x256, 4-stage ring.  The grouped
-// (MoE) variant walks a tile list over (expert, 128-row tile, 256-col tile).
+// in TMEM for the whole K loop.  Tile 128x256, 4-stage ring, 8 epilogue
+// warps.  The grouped (MoE) variant walks a tile list over (expert, 128-row
+// tile, 256-col tile).
 //
 // Every wait is bounded (see mbar_wait_bounded); on expiry the kernel records
-// FP8_ERR_TIMEOUT, lets in-flight copies and MMAs land, frees TMEM, and exits.
+// FP8_ERR_TIMEOUT, stops issuing work, and exits through the same teardown.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -48,22 +47,25 @@ constexpr int kEpiThreads = 256;
 constexpr int kMaxStages = 6;
 constexpr int kMaxGroups = 1024;
 
-// blockwise kernel: each ring stage holds K = 256 (two 128-wide scale blocks,
-// A and B as two 128-byte-wide swizzled halves each) so that the MMA thread
-// waits on one barrier per 8 MMAs (512 tensor-core cycles); the four TMEM
-// partial buffers of 128 columns are used as two pairs, one pair per stage.
-constexpr int kBwBN = 128;
-constexpr int kBwStages = 3;
-constexpr uint32_t kBwHalfBytes = 128 * BK;           // 16 KB: 128 rows x 128 bytes
-constexpr uint32_t kBwStageBytes = 4 * kBwHalfBytes;  // A0 A1 B0 B1 = 64 KB
+// blockwise kernel: a cluster of two CTAs on neighbouring SMs computes a
+// 256x256 tile with tcgen05.mma.cta_group::2 (M=256, N=128, two N halves per
+// K step).  Each CTA stages its own 128 rows of A and, of each 128-column N
+// half, the 64 rows of B it contributes, so an SM takes in 32 KB per
+// 128x256x128 of work -- half of what a 128x128 tile needs.  Each CTA keeps
+// a 128x256 fp32 result in its 16 epilogue warps (64 columns each); the
+// per-K-block partials P live in two TMEM sets of 256 columns, so the
+// tensor cores fill one set while the epilogue promotes the other.
+constexpr int kBwBN = 256;                               // tile columns (both CTAs)
+constexpr int kBwStages = 6;                             // one 128-wide K block per stage
+constexpr uint32_t kBwABytes = 128 * BK;                 // 16 KB: this CTA's 128 rows of A
+constexpr uint32_t kBwBQuarter = 64 * BK;                // 8 KB: 64 rows of B (one N half's share)
+constexpr uint32_t kBwStageBytes = kBwABytes + 2 * kBwBQuarter;  // 32 KB
 constexpr uint32_t kBwTmemCols = 512;
-constexpr int kBwEpiWarps = 8;                           // 2 per TMEM lane quarter
-constexpr int kBwLoaderWarp = kEpiWarp0 + kBwEpiWarps;     // fills the scale ring
-constexpr int kBwThreads = (kBwLoaderWarp + 1) * 32;
-constexpr int kBwSlices = kBwEpiWarps / 4;                // column slices of a row
-constexpr int kBwCols = kBwBN / kBwSlices;                // columns per epilogue thread
-constexpr int kBwChunks = kBwCols / 16;
-constexpr uint32_t kIdescBlockwise = idesc_f8f6f4(BM, kBwBN);
+constexpr int kBwEpiWarps = 16;                          // 4 per TMEM lane quarter
+constexpr int kBwLoaderWarp = kEpiWarp0 + kBwEpiWarps;   // fills the scale ring
+constexpr int kBwThreads = (kBwLoaderWarp + 1) * 32;     // 608
+constexpr int kBwCols = kBwBN / (kBwEpiWarps / 4);       // 64 columns per epilogue thread
+constexpr uint32_t kIdescBlockwise = idesc_f8f6f4(2 * BM, 128);
 
 // MX kernel
 constexpr int kMxBN = 256;
@@ -84,13 +86,13 @@ struct alignas(16) Barriers {
 };
 
 // blockwise kernel only (16-byte aligned: float4 reads and 16-byte cp.async)
-constexpr int kBwScaleSlots = 6;
+constexpr int kBwScaleSlots = 8;
 struct alignas(16) BwShared {
     uint64_t sc_full[kBwScaleSlots];   // scale slot filled (32 cp.async arrivals of the loader warp)
     uint64_t sc_empty[kBwScaleSlots];  // scale slot read by all epilogue warps
-    float amax_xch[kBwSlices][128];    // fused quantization: per-slice row maxima
-    float sa[kBwScaleSlots][2][128];   // per pair: row scales of the tile's 128 rows, 2 K blocks
-    float sb[kBwScaleSlots][2][128];   // per pair: column scales (WGrad) or the block scale at [.][k][0]
+    float amax_xch[kBwEpiWarps / 4][128];  // fused quantization: per-warp row maxima
+    float sa[kBwScaleSlots][128];      // per K block: row scales of this CTA's 128 rows
+    float sb[kBwScaleSlots][kBwBN];    // per K block: column scales (WGrad) or the two block scales at [.][0..1]
 };
 
 constexpr size_t kSmemBlockwise = 1024 + (size_t)kBwStages * kBwStageBytes + sizeof(Barriers) + sizeof(BwShared);
@@ -181,29 +183,9 @@ struct BwParams {
     uint8_t* q_codes;
     float* q_scales;
     StatusBlock* st;
-    int tiles_m, tiles_n;
-    int d_v8, q_v8;  // D rows / code rows allow 32-byte stores
+    int tiles_m, tiles_n;  // 256x256 cluster tiles
+    int d_v8, q_v8;        // D rows / code rows allow 32-byte stores
 };
-
-// Global pair index j of this CTA -> its tile and pair-within-tile.  Tiles
-// are visited blockIdx.x, blockIdx.x + gridDim.x, ...; every tile has
-// npairs = ceil(KB/2) pairs.
-struct PairCoord {
-    bool valid;
-    int tm, tn, p, nk;  // nk: K blocks in this pair (1 or 2)
-};
-
-__device__ __forceinline__ PairCoord bw_pair(int j, int npairs, int KB, int tiles_n, int num_tiles) {
-    PairCoord c;
-    const int i = j / npairs;
-    c.p = j - i * npairs;
-    const int tile = blockIdx.x + i * gridDim.x;
-    c.valid = tile < num_tiles;
-    c.tm = tile / tiles_n;
-    c.tn = tile - c.tm * tiles_n;
-    c.nk = KB - 2 * c.p >= 2 ? 2 : 1;
-    return c;
-}
 
 // acc[2i..2i+1] += (P * c) with packed fp32x2 FMAs, 16 columns
 __device__ __forceinline__ void promote16x2(float* acc, const uint32_t (&r)[16], float c) {
@@ -233,6 +215,13 @@ __device__ __forceinline__ void promote16x2_cols(float* acc, const uint32_t (&r)
     }
 }
 
+// Cluster c of C visits the 256x256 tiles c, c + C, ...; its g-th K block
+// (over all its tiles) is K block g % KB of tile c + (g / KB) * C.
+__device__ __forceinline__ void bw_tile(int t, int tiles_n, int& tm, int& tn) {
+    tm = t / tiles_n;
+    tn = t - tm * tiles_n;
+}
+
 __global__ void __launch_bounds__(kBwThreads, 1)
     k_gemm_blockwise(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const BwParams p) {
@@ -243,19 +232,22 @@ __global__ void __launch_bounds__(kBwThreads, 1)
     volatile int* abort = &bar->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = p.K / BK;
-    const int npairs = (KB + 1) / 2;
     const int num_tiles = p.tiles_m * p.tiles_n;
-    const int my_tiles = (int)blockIdx.x < num_tiles ? (num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int total_pairs = my_tiles * npairs;
+    const int cid = (int)(blockIdx.x >> 1), ncl = (int)(gridDim.x >> 1);
+    const int my_tiles = cid < num_tiles ? (num_tiles - 1 - cid) / ncl + 1 : 0;
+    const int total = my_tiles * KB;          // K blocks this CTA pair computes
+    const uint32_t rank = cluster_ctarank();  // 0: leader CTA (issues the MMAs)
+    const int row0 = BM * (int)rank;          // this CTA's rows within the 256-row tile
 
     if (threadIdx.x == 0) {
-        // full[s]: the producer's expect_tx arrival plus one arrival from each
-        // epilogue warp granting the TMEM pair (and, for WGrad, its scales)
+        // full[s] (used in the leader only): the leader producer's expect_tx
+        // arrival for both CTAs' bytes plus one arrival from each epilogue
+        // warp of both CTAs granting its share of the TMEM set to the stage
         for (int s = 0; s < kBwStages; ++s) {
-            mbar_init(&bar->full[s], 1 + kBwEpiWarps);
+            mbar_init(&bar->full[s], 1 + 2 * kBwEpiWarps);
             mbar_init(&bar->empty[s], 1);
         }
-        for (int b = 0; b < 4; ++b) mbar_init(&bar->acc_full[b], 1);  // [2*(pair&1) + half]
+        for (int b = 0; b < 2; ++b) mbar_init(&bar->acc_full[b], 1);
         for (int i = 0; i < kBwScaleSlots; ++i) {
             mbar_init(&bws->sc_full[i], 32);
             mbar_init(&bws->sc_empty[i], kBwEpiWarps);
@@ -268,205 +260,164 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
     }
-    if (warp == 1) tmem_alloc(&bar->tmem_base, kBwTmemCols);
+    if (warp == 1) tmem_alloc_pair(&bar->tmem_base, kBwTmemCols);
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // barriers initialised and TMEM allocated in both CTAs
     tc_fence_after();
     const uint32_t tmem = bar->tmem_base;
+    const uint32_t full_leader = mapa_shared(&bar->full[0], 0);  // + 8 * stage
 
     if (warp == 0) {
         if (lane == 0) {
-            uint32_t fills[kBwStages] = {0, 0, 0};
-            bool ok = true;
-            for (int j = 0; j < total_pairs && ok; ++j) {
-                const PairCoord c = bw_pair(j, npairs, KB, p.tiles_n, num_tiles);
-                const int s = j % kBwStages;
-                if (!mbar_wait_bounded(&bar->empty[s], ((j / kBwStages) & 1) ^ 1, abort, p.st, 1)) {
-                    ok = false;
-                    break;
-                }
+            int tm = 0, tn = 0, kb = 0, ti = 0;
+            for (int g = 0; g < total; ++g) {
+                if (kb == 0) bw_tile(cid + ti * ncl, p.tiles_n, tm, tn);
+                const int s = g % kBwStages;
+                if (!mbar_wait_bounded(&bar->empty[s], ((g / kBwStages) & 1) ^ 1, abort, p.st, 1)) break;
                 uint8_t* stage = smem + s * kBwStageBytes;
-                mbar_arrive_expect_tx(&bar->full[s], (uint32_t)c.nk * 2 * kBwHalfBytes);
-                const int k0 = 2 * c.p * BK;
-                tma_load_2d(stage, &tmA, &bar->full[s], k0, c.tm * BM);
-                tma_load_2d(stage + 2 * kBwHalfBytes, &tmB, &bar->full[s], k0, c.tn * kBwBN);
-                if (c.nk == 2) {
-                    tma_load_2d(stage + kBwHalfBytes, &tmA, &bar->full[s], k0 + BK, c.tm * BM);
-                    tma_load_2d(stage + 3 * kBwHalfBytes, &tmB, &bar->full[s], k0 + BK, c.tn * kBwBN);
+                if (rank == 0) mbar_arrive_expect_tx(&bar->full[s], 2 * kBwStageBytes);
+                const uint32_t fb = full_leader + 8u * (uint32_t)s;
+                const int k0 = kb * BK, by = tn * kBwBN + 64 * (int)rank;
+                tma_load_2d_pair(stage, &tmA, fb, k0, tm * 2 * BM + row0);
+                tma_load_2d_pair(stage + kBwABytes, &tmB, fb, k0, by);
+                tma_load_2d_pair(stage + kBwABytes + kBwBQuarter, &tmB, fb, k0, by + 128);
+                if (++kb == KB) {
+                    kb = 0;
+                    ++ti;
                 }
-                ++fills[s];
             }
-            if (!ok)
-                for (int i = 0; i < kBwStages; ++i)
-                    if (fills[i]) mbar_wait_drain(&bar->full[i], (fills[i] - 1) & 1, p.st);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            for (int j = 0; j < total_pairs; ++j) {
-                const PairCoord c = bw_pair(j, npairs, KB, p.tiles_n, num_tiles);
-                const int s = j % kBwStages;
-                if (!mbar_wait_bounded(&bar->full[s], (j / kBwStages) & 1, abort, p.st, 3)) break;
+        if (lane == 0 && rank == 0) {
+            for (int g = 0; g < total; ++g) {
+                const int s = g % kBwStages;
+                if (!mbar_wait_bounded(&bar->full[s], (g / kBwStages) & 1, abort, p.st, 3)) break;
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(smem + s * kBwStageBytes);
-                const uint32_t pbuf = tmem + (uint32_t)((j & 1) * 2 * kBwBN);
+                const uint64_t adesc = sdesc_k_sw128(a_addr);
+                const uint32_t pset = tmem + (uint32_t)((g & 1) * kBwBN);
 #pragma unroll
-                for (int hk = 0; hk < 2; ++hk) {
-                    if (hk < c.nk) {
-                        const uint64_t adesc = sdesc_k_sw128(a_addr + hk * kBwHalfBytes);
-                        const uint64_t bdesc = sdesc_k_sw128(a_addr + (2 + hk) * kBwHalfBytes);
+                for (int nh = 0; nh < 2; ++nh) {
+                    const uint64_t bdesc = sdesc_k_sw128(a_addr + kBwABytes + nh * kBwBQuarter);
 #pragma unroll
-                        for (int k = 0; k < BK / 32; ++k)
-                            tc_mma_f8f6f4(pbuf + (uint32_t)(hk * kBwBN), adesc + 2 * k, bdesc + 2 * k, kIdescBlockwise,
-                                          k > 0 ? 1u : 0u);
-                    }
-                    if (hk == 1) tc_commit(&bar->empty[s]);
-                    // each half is handed to the epilogue as soon as it is done
-                    // (a half-pair at an odd-K tail still commits, keeping phases aligned)
-                    tc_commit(&bar->acc_full[2 * (j & 1) + hk]);
+                    for (int k = 0; k < BK / 32; ++k)
+                        tc_mma_f8f6f4_pair(pset + (uint32_t)(128 * nh), adesc + 2 * k, bdesc + 2 * k, kIdescBlockwise,
+                                           k > 0 ? 1u : 0u);
                 }
+                tc_commit_pair(&bar->empty[s], 3);        // stage free in both CTAs
+                tc_commit_pair(&bar->acc_full[g & 1], 3);  // P set ready in both CTAs
             }
-            tc_commit(&bar->drain);
+            tc_commit_pair(&bar->drain, 1);
             mbar_wait_drain(&bar->drain, 0, p.st);
         }
     } else if (warp == kBwLoaderWarp) {
-        // scale loader: per pair, the row scales of the tile's 128 rows and
-        // the column (WGrad) or block scales of its two K blocks, by cp.async
-        // into ring slot j%6; each lane's copies complete onto sc_full.
-        int ti = 0, pp = 0, tm = 0, tn = 0;
-        for (int j = 0; j < total_pairs; ++j) {
-            if (pp == 0) {
-                const int tile = blockIdx.x + ti * gridDim.x;
-                tm = tile / p.tiles_n;
-                tn = tile - tm * p.tiles_n;
+        // scale loader: per K block, the row scales of this CTA's 128 rows and
+        // the tile's column (WGrad) or two block scales, by cp.async into ring
+        // slot g % 8; each lane's copies complete onto sc_full.
+        const int nblocks = p.N / 128;
+        int tm = 0, tn = 0, kb = 0, ti = 0;
+        for (int g = 0; g < total; ++g) {
+            if (kb == 0) bw_tile(cid + ti * ncl, p.tiles_n, tm, tn);
+            const int slot = g % kBwScaleSlots;
+            if (!mbar_wait_bounded(&bws->sc_empty[slot], ((g / kBwScaleSlots) & 1) ^ 1, abort, p.st, 7)) break;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int m = tm * 2 * BM + row0 + 4 * lane + i;
+                const bool ok = m < p.M;
+                const float* src = ok ? p.sa + (size_t)kb * p.M + m : p.sa;
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(&bws->sa[slot][4 * lane + i])),
+                             "l"(src), "r"(ok ? 4 : 0)
+                             : "memory");
             }
-            const int slot = j % kBwScaleSlots;
-            if (!mbar_wait_bounded(&bws->sc_empty[slot], ((j / kBwScaleSlots) & 1) ^ 1, abort, p.st, 7)) break;
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int kb = 2 * pp + k;
-                const bool kok = kb < KB;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int m = tm * BM + 4 * lane + i;
-                    const bool ok = kok && m < p.M;
-                    const float* src = ok ? p.sa + (size_t)kb * p.M + m : p.sa;
-                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
-                                     smem_u32(&bws->sa[slot][k][4 * lane + i])),
+            if (!p.sb_per_row) {
+                if (lane < 2) {
+                    const int nb = 2 * tn + lane;
+                    const bool ok = nb < nblocks;
+                    const float* src = ok ? p.sb + (size_t)nb * KB + kb : p.sb;
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(&bws->sb[slot][lane])),
                                  "l"(src), "r"(ok ? 4 : 0)
                                  : "memory");
                 }
-                if (!p.sb_per_row) {
-                    if (lane == 0) {
-                        const float* src = kok ? p.sb + (size_t)tn * KB + kb : p.sb;
-                        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(&bws->sb[slot][k][0])),
-                                     "l"(src), "r"(kok ? 4 : 0)
-                                     : "memory");
-                    }
-                } else {
-                    const float* src = kok ? p.sb + (size_t)kb * p.N + tn * kBwBN + 4 * lane : p.sb;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int col = tn * kBwBN + 8 * lane + 4 * i;
+                    const bool ok = col < p.N;
+                    const float* src = ok ? p.sb + (size_t)kb * p.N + col : p.sb;
                     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                                     smem_u32(&bws->sb[slot][k][4 * lane])),
-                                 "l"(src), "r"(kok ? 16 : 0)
+                                     smem_u32(&bws->sb[slot][8 * lane + 4 * i])),
+                                 "l"(src), "r"(ok ? 16 : 0)
                                  : "memory");
                 }
             }
             asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&bws->sc_full[slot]))
                          : "memory");
-            if (++pp == npairs) {
-                pp = 0;
+            if (++kb == KB) {
+                kb = 0;
                 ++ti;
             }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
     } else {
-        // epilogue: warp (q = warp%4, h) promotes rows 32q.. , columns kBwCols*h ..
+        // epilogue: warp (q = warp % 4, h) promotes rows 32q.. of this CTA,
+        // tile columns 64h .. 64h+63 (N half h / 2)
         const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
-        const int ew = warp - kEpiWarp0;
         const int rl = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        (void)ew;
-        // grant the TMEM pairs of pairs 0 and 1
+        // grant the TMEM sets of K blocks 0 and 1
         if (lane == 0) {
-            mbar_arrive(&bar->full[0]);
-            mbar_arrive(&bar->full[1]);
+            mbar_arrive_cluster(full_leader);
+            mbar_arrive_cluster(full_leader + 8u);
         }
 
         bool ok = true;
         for (int ti = 0; ti < my_tiles && ok; ++ti) {
-        const int tile = blockIdx.x + ti * gridDim.x;
-        const int ctm = tile / p.tiles_n, ctn = tile - ctm * p.tiles_n;
-        float acc[kBwCols];
+            int ctm, ctn;
+            bw_tile(cid + ti * ncl, p.tiles_n, ctm, ctn);
+            float acc[kBwCols];
 #pragma unroll
-        for (int i = 0; i < kBwCols; ++i) acc[i] = 0.0f;
-        for (int pp = 0; pp < npairs; ++pp) {
-            const int j = ti * npairs + pp;
-            PairCoord c;
-            c.p = pp;
-            c.nk = KB - 2 * pp >= 2 ? 2 : 1;
-            const int slot = j % kBwScaleSlots;
-            if (!mbar_wait_bounded(&bws->sc_full[slot], (j / kBwScaleSlots) & 1, abort, p.st, 5) ||
-                !mbar_wait_bounded(&bar->acc_full[2 * (j & 1)], (j >> 1) & 1, abort, p.st, 4)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t tb = tmem + lane_base + (uint32_t)((j & 1) * 2 * kBwBN + kBwCols * h);
-            uint32_t r[kBwChunks][16];
-#pragma unroll
-            for (int cc = 0; cc < kBwChunks; ++cc) tmem_ld_32x32b_x16(tb + 16 * cc, r[cc]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int cc = 0; cc < kBwChunks; ++cc) reg_fence16(r[cc]);
-            const float sa0 = bws->sa[slot][0][rl], sa1 = bws->sa[slot][1][rl];
-            const float* sbs0 = &bws->sb[slot][0][kBwCols * h];
-            const float* sbs1 = &bws->sb[slot][1][kBwCols * h];
-            if (!p.sb_per_row) {
-                const float cs = sa0 * bws->sb[slot][0][0];
-#pragma unroll
-                for (int cc = 0; cc < kBwChunks; ++cc) promote16x2(acc + 16 * cc, r[cc], cs);
-            } else {
-#pragma unroll
-                for (int cc = 0; cc < kBwChunks; ++cc) promote16x2_cols(acc + 16 * cc, r[cc], sbs0 + 16 * cc, sa0);
-            }
-            if (c.nk == 2) {
-                if (!mbar_wait_bounded(&bar->acc_full[2 * (j & 1) + 1], (j >> 1) & 1, abort, p.st, 6)) {
+            for (int i = 0; i < kBwCols; ++i) acc[i] = 0.0f;
+            for (int kb = 0; kb < KB; ++kb) {
+                const int g = ti * KB + kb;
+                const int slot = g % kBwScaleSlots;
+                if (!mbar_wait_bounded(&bws->sc_full[slot], (g / kBwScaleSlots) & 1, abort, p.st, 5) ||
+                    !mbar_wait_bounded(&bar->acc_full[g & 1], (g >> 1) & 1, abort, p.st, 4)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const uint32_t tb = tmem + lane_base + (uint32_t)((g & 1) * kBwBN + kBwCols * h);
+                const float sa = bws->sa[slot][rl];
+                const float cs = sa * bws->sb[slot][h >> 1];
+                const float* sbc = &bws->sb[slot][kBwCols * h];
 #pragma unroll
-                for (int cc = 0; cc < kBwChunks; ++cc) tmem_ld_32x32b_x16(tb + kBwBN + 16 * cc, r[cc]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int cc = 0; cc < kBwChunks; ++cc) reg_fence16(r[cc]);
-            }
-            // the pair's TMEM is read: grant it to pair j+2 (whose stage is j+2)
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0 && j + 2 < total_pairs) mbar_arrive(&bar->full[(j + 2) % kBwStages]);
-            if (c.nk == 2) {
-                if (!p.sb_per_row) {
-                    const float cs = sa1 * bws->sb[slot][1][0];
-#pragma unroll
-                    for (int cc = 0; cc < kBwChunks; ++cc) promote16x2(acc + 16 * cc, r[cc], cs);
-                } else {
-#pragma unroll
-                    for (int cc = 0; cc < kBwChunks; ++cc)
-                        promote16x2_cols(acc + 16 * cc, r[cc], sbs1 + 16 * cc, sa1);
+                for (int cc = 0; cc < kBwCols / 16; ++cc) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(tb + 16 * cc, r);
+                    tmem_ld_wait();
+                    reg_fence16(r);
+                    if (!p.sb_per_row)
+                        promote16x2(acc + 16 * cc, r, cs);
+                    else
+                        promote16x2_cols(acc + 16 * cc, r, sbc + 16 * cc, sa);
+                }
+                // this warp's share of the TMEM set is read: grant it to K
+                // block g + 2, and hand the scale slot back to the loader
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (g + 2 < total) mbar_arrive_cluster(full_leader + 8u * (uint32_t)((g + 2) % kBwStages));
+                    mbar_arrive(&bws->sc_empty[slot]);
                 }
             }
-            // the scale slot is read: hand it back to the loader warp
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bws->sc_empty[slot]);
-        }
-        if (!ok) break;
-        {
+            if (!ok) break;
+
             // tile done: store D (and the fused 1x128 quantization)
-            const int m = ctm * BM + rl;
+            const int m = ctm * 2 * BM + row0 + rl;
             const int ncol0 = ctn * kBwBN + kBwCols * h;
-            const bool mvalid = m < p.M;
+            const bool valid = m < p.M && ncol0 < p.N;  // N % 128 == 0: a warp's columns are all in or all out
             if (p.d_f32) {
-                if (mvalid) {
+                if (valid) {
                     float* drow = reinterpret_cast<float*>(p.D) + (size_t)m * p.ldd + ncol0;
                     if (p.d_v8) {
 #pragma unroll
@@ -487,7 +438,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                 uint32_t packed[kBwCols / 2];
 #pragma unroll
                 for (int i = 0; i < kBwCols / 2; ++i) packed[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
-                if (mvalid) {
+                if (valid) {
                     uint16_t* drow = reinterpret_cast<uint16_t*>(p.D) + (size_t)m * p.ldd + ncol0;
                     if (p.d_v8) {
 #pragma unroll
@@ -500,44 +451,33 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                     }
                 }
                 if (p.q_codes != nullptr) {
-                    // a 1x128 group spans the kBwSlices warps of this lane
-                    // quarter: exchange the slice maxima through shared memory
+                    // a 1x128 group of a row spans warps h and h ^ 1 of this
+                    // lane quarter: exchange their maxima through shared memory
                     float a = 0.0f;
 #pragma unroll
                     for (int i = 0; i < kBwCols / 2; ++i)
                         a = fmaxf(a, fmaxf(fabsf(bf16_lo(packed[i])), fabsf(bf16_hi(packed[i]))));
                     bws->amax_xch[h][rl] = a;
-                    asm volatile("bar.sync %0, %1;" ::"r"(1 + q), "r"(32 * kBwSlices) : "memory");
-#pragma unroll
-                    for (int o = 0; o < kBwSlices; ++o) a = fmaxf(a, bws->amax_xch[o][rl]);
-                    asm volatile("bar.sync %0, %1;" ::"r"(1 + q), "r"(32 * kBwSlices) : "memory");
+                    const int bar_id = 1 + 2 * q + (h >> 1);
+                    asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(64) : "memory");
+                    a = fmaxf(a, bws->amax_xch[h ^ 1][rl]);
+                    asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(64) : "memory");
                     const float sc = group_scale(a);
-                    if (mvalid) {
+                    if (valid) {
                         uint8_t* codes = p.q_codes + (size_t)m * p.N + ncol0;
                         uint32_t cw[kBwCols / 4];
 #pragma unroll
-                        for (int i = 0; i < kBwCols / 16; ++i) {
-                            float f0[8], f1[8];
+                        for (int i = 0; i < kBwCols / 8; ++i) {
+                            float f[8];
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                f0[2 * k] = bf16_lo(packed[8 * i + k]);
-                                f0[2 * k + 1] = bf16_hi(packed[8 * i + k]);
-                                f1[2 * k] = bf16_lo(packed[8 * i + 4 + k]);
-                                f1[2 * k + 1] = bf16_hi(packed[8 * i + 4 + k]);
+                                f[2 * k] = bf16_lo(packed[4 * i + k]);
+                                f[2 * k + 1] = bf16_hi(packed[4 * i + k]);
                             }
-                            uint4 w;
-                            w.x = e4m3x2(__fdiv_rn(f0[0], sc), __fdiv_rn(f0[1], sc)) |
-                                  (e4m3x2(__fdiv_rn(f0[2], sc), __fdiv_rn(f0[3], sc)) << 16);
-                            w.y = e4m3x2(__fdiv_rn(f0[4], sc), __fdiv_rn(f0[5], sc)) |
-                                  (e4m3x2(__fdiv_rn(f0[6], sc), __fdiv_rn(f0[7], sc)) << 16);
-                            w.z = e4m3x2(__fdiv_rn(f1[0], sc), __fdiv_rn(f1[1], sc)) |
-                                  (e4m3x2(__fdiv_rn(f1[2], sc), __fdiv_rn(f1[3], sc)) << 16);
-                            w.w = e4m3x2(__fdiv_rn(f1[4], sc), __fdiv_rn(f1[5], sc)) |
-                                  (e4m3x2(__fdiv_rn(f1[6], sc), __fdiv_rn(f1[7], sc)) << 16);
-                            cw[4 * i] = w.x;
-                            cw[4 * i + 1] = w.y;
-                            cw[4 * i + 2] = w.z;
-                            cw[4 * i + 3] = w.w;
+                            cw[2 * i] = e4m3x2(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc)) |
+                                        (e4m3x2(__fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc)) << 16);
+                            cw[2 * i + 1] = e4m3x2(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc)) |
+                                            (e4m3x2(__fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc)) << 16);
                         }
                         if (p.q_v8) {
 #pragma unroll
@@ -548,20 +488,22 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                                 reinterpret_cast<uint4*>(codes)[i] =
                                     make_uint4(cw[4 * i], cw[4 * i + 1], cw[4 * i + 2], cw[4 * i + 3]);
                         }
-                        if (h == 0) p.q_scales[(size_t)ctn * p.M + m] = sc;
+                        if ((h & 1) == 0) p.q_scales[(size_t)(ncol0 / 128) * p.M + m] = sc;
                     }
                 }
             }
         }
-        }
     }
 
+    // neither CTA leaves while the other may still signal its barriers or
+    // the leader's MMAs may still write its TMEM
+    __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, kBwTmemCols);
+        tmem_dealloc_pair(tmem, kBwTmemCols);
     }
 }
 
@@ -846,7 +788,7 @@ cudaError_t launch_gemm_blockwise(const GemmBlockwiseArgs& a, StatusBlock* statu
     if (a.M == 0 || a.N == 0) return cudaSuccess;
     CUtensorMap tmA, tmB;
     if (!make_map(&tmA, a.a_codes, (uint64_t)a.K, (uint64_t)a.M, BM) ||
-        !make_map(&tmB, a.b_codes, (uint64_t)a.K, (uint64_t)a.N, kBwBN))
+        !make_map(&tmB, a.b_codes, (uint64_t)a.K, (uint64_t)a.N, 64))
         return cudaErrorInvalidValue;
     BwParams p;
     p.sa = a.sa;
@@ -861,18 +803,41 @@ cudaError_t launch_gemm_blockwise(const GemmBlockwiseArgs& a, StatusBlock* statu
     p.q_codes = a.q_codes;
     p.q_scales = a.q_scales;
     p.st = status;
-    p.tiles_m = (int)((a.M + BM - 1) / BM);
+    p.tiles_m = (int)((a.M + 2 * BM - 1) / (2 * BM));
     p.tiles_n = (int)((a.N + kBwBN - 1) / kBwBN);
     const int64_t row_bytes = a.ldd * (a.d_f32 ? 4 : 2);
     p.d_v8 = (reinterpret_cast<uintptr_t>(a.D) % 32 == 0) && (row_bytes % 32 == 0);
     p.q_v8 = reinterpret_cast<uintptr_t>(a.q_codes) % 32 == 0;
     const int tiles = p.tiles_m * p.tiles_n;
-    const int grid = tiles < sm_count() ? tiles : sm_count();
     cudaError_t e = cudaFuncSetAttribute(k_gemm_blockwise, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBlockwise);
     if (e != cudaSuccess) return e;
-    k_gemm_blockwise<<<grid, kBwThreads, kSmemBlockwise, st>>>(tmA, tmB, p);
-    return cudaGetLastError();
+    // persistent grid of CTA pairs (clusters of 2): as many as can be resident
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (unsigned)tiles);
+    cfg.blockDim = dim3(kBwThreads);
+    cfg.dynamicSmemBytes = kSmemBlockwise;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static int max_pairs[64] = {0};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int& mp = max_pairs[dev & 63];
+    if (mp <= 0) {
+        e = cudaOccupancyMaxActiveClusters(&mp, k_gemm_blockwise, &cfg);
+        if (e != cudaSuccess) return e;
+        if (mp <= 0) return cudaErrorInvalidConfiguration;
+    }
+    const int pairs = tiles < mp ? tiles : mp;
+    cfg.gridDim = dim3(2 * (unsigned)pairs);
+    return cudaLaunchKernelEx(&cfg, k_gemm_blockwise, tmA, tmB, p);
 }
 
 cudaError_t launch_gemm_mx(const GemmMxArgs& a, StatusBlock* status, cudaStream_t st) {
@@ -906,3 +871,4 @@ cudaError_t launch_gemm_mx(const GemmMxArgs& a, StatusBlock* status, cudaStream_
 }
 
 }  // namespace fp8bs
+
