@@ -100,11 +100,18 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ timing helpers
 class Flusher:
+    """Writes a buffer larger than L2, then reads another one, so that the
+    timed kernel starts with no data of its own and no dirty lines in L2
+    (the write-backs of the flush itself stay outside the timed region)."""
+
     def __init__(self, dev):
         self.buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.rbuf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def __call__(self):
         self.buf.fill_(1.0)
+        torch.sum(self.rbuf, dim=0, out=self.sink)
 
 
 def time_kernel(fn, flush, reps, warmup=3):

@@ -63,6 +63,36 @@ __device__ __forceinline__ float group_scale(float amax) {
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
+// x / s correctly rounded, for the quotients of the blockwise quantizers:
+// x a bf16 value and s = RN(amax / 448) of the group maximum amax >= |x|.
+// For s >= 2^-100 it takes Markstein's FMA correction of the product with the
+// correctly rounded reciprocal (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990): q0 = RN(x r), e = x - s q0 (exact by FMA), q = RN(q0 + e r), with the
+// sign of x so that -0 stays -0.  An exhaustive host check over every bf16 x
+// and every bf16 group maximum gives the E4M3 code of the IEEE quotient in
+// every case (the quotient bits differ only below 2^-11, where the code is
+// zero either way); smaller or non-finite s take the IEEE division.
+struct Divider {
+    float s, r;
+    bool fast;
+};
+
+__device__ __forceinline__ Divider make_divider(float s) {
+    Divider d;
+    d.s = s;
+    d.r = __frcp_rn(s);
+    d.fast = s >= 0x1p-100f && s <= 3.402823466e38f;
+    return d;
+}
+
+__device__ __forceinline__ float quotient(const Divider& d, float x) {
+    if (!d.fast) return __fdiv_rn(x, d.s);
+    const float q0 = __fmul_rn(x, d.r);
+    const float e = __fmaf_rn(-d.s, q0, x);
+    return copysignf(__fmaf_rn(e, d.r, q0), x);
+}
+
 // MX shared exponent e = clamp(floor(log2 amax) - 8, -127, 127) from the fp32
 // bit fields (no log2 evaluation); -127 for an all-zero block.
 __device__ __forceinline__ int mx_exponent(float amax) {

@@ -463,6 +463,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                     a = fmaxf(a, bws->amax_xch[h ^ 1][rl]);
                     asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(64) : "memory");
                     const float sc = group_scale(a);
+                    const Divider dv = make_divider(sc);
                     if (valid) {
                         uint8_t* codes = p.q_codes + (size_t)m * p.N + ncol0;
                         uint32_t cw[kBwCols / 4];
@@ -474,10 +475,10 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                                 f[2 * k] = bf16_lo(packed[4 * i + k]);
                                 f[2 * k + 1] = bf16_hi(packed[4 * i + k]);
                             }
-                            cw[2 * i] = e4m3x2(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc)) |
-                                        (e4m3x2(__fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc)) << 16);
-                            cw[2 * i + 1] = e4m3x2(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc)) |
-                                            (e4m3x2(__fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc)) << 16);
+                            cw[2 * i] = e4m3x2(quotient(dv, f[0]), quotient(dv, f[1])) |
+                                        (e4m3x2(quotient(dv, f[2]), quotient(dv, f[3])) << 16);
+                            cw[2 * i + 1] = e4m3x2(quotient(dv, f[4]), quotient(dv, f[5])) |
+                                            (e4m3x2(quotient(dv, f[6]), quotient(dv, f[7])) << 16);
                         }
                         if (p.q_v8) {
 #pragma unroll

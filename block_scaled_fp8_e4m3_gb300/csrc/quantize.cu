@@ -40,11 +40,11 @@ __device__ __forceinline__ float amax8(const float (&f)[8]) {
     return a;
 }
 
-// 8 values divided by s (IEEE fp32 division) and encoded: 8 codes in two words.
-__device__ __forceinline__ uint2 encode8_div(const float (&f)[8], float s) {
+// 8 values divided by s (the IEEE fp32 quotient) and encoded: 8 codes in two words.
+__device__ __forceinline__ uint2 encode8_div(const float (&f)[8], const Divider& d) {
     uint2 r;
-    r.x = e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) | (e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
-    r.y = e4m3x2(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s)) | (e4m3x2(__fdiv_rn(f[6], s), __fdiv_rn(f[7], s)) << 16);
+    r.x = e4m3x2(quotient(d, f[0]), quotient(d, f[1])) | (e4m3x2(quotient(d, f[2]), quotient(d, f[3])) << 16);
+    r.y = e4m3x2(quotient(d, f[4]), quotient(d, f[5])) | (e4m3x2(quotient(d, f[6]), quotient(d, f[7])) << 16);
     return r;
 }
 
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(256) k_quant_group_k(const uint16_t* __restric
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
         const float s = group_scale(a);
         if (row_ok && g < G) {
-            const uint2 c = encode8_div(f, s);
+            const uint2 c = encode8_div(f, make_divider(s));
             *reinterpret_cast<uint2*>(codes + row * K + g * 128 + sub * 8) = c;
             if (sub == 0) scales[g * M + row] = s;
         }
@@ -155,9 +155,10 @@ __global__ void __launch_bounds__(256) k_quant_group_m(const uint16_t* __restric
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const float s = col_scale[chunk * 8 + j];
+        const Divider dv = make_divider(s);
         float q[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) q[i] = __fdiv_rn(f[i][j], s);
+        for (int i = 0; i < 4; ++i) q[i] = quotient(dv, f[i][j]);
         tile[(chunk * 8 + j) * 33 + quad] = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
     }
     __syncthreads();
@@ -220,11 +221,12 @@ __global__ void __launch_bounds__(256) k_quant_block(const uint16_t* __restrict_
         scales[nb * KB + kb] = s;
         if (scales_t) scales_t[kb * NB + nb] = s;
     }
+    const Divider dv = make_divider(s);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         float f[8];
         unpack8(v[i], f);
-        const uint2 c = encode8_div(f, s);
+        const uint2 c = encode8_div(f, dv);
         *reinterpret_cast<uint2*>(codes + (n0 + rg * 8 + i) * K + k0 + chunk * 8) = c;
         if (codes_t) *reinterpret_cast<uint2*>(tile + (rg * 8 + i) * kStride + chunk * 8) = c;
     }
