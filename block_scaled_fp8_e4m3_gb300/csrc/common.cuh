@@ -58,9 +58,22 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
     return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
-// Blockwise scale s = amax / 448 (IEEE fp32 division); 1 for an all-zero group.
+// Blockwise scale s = amax / 448 (IEEE fp32 quotient); 1 for an all-zero group.
 __device__ __forceinline__ float group_scale(float amax) {
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+}
+
+// The same scale for a group maximum that is a bf16 value: Markstein's FMA
+// correction of amax * RN(1/448) (see quotient() below); a host check over
+// every positive finite bf16 value gives the IEEE quotient bit for bit.  The
+// maximum (a fmaxf reduction from 0) is never NaN; an infinite one gives
+// inf / 448 = inf.
+__device__ __forceinline__ float group_scale_bf16(float amax) {
+    constexpr float kInv448 = 1.0f / 448.0f;
+    const float q0 = __fmul_rn(amax, kInv448);
+    const float e = __fmaf_rn(-448.0f, q0, amax);
+    const float s = __fmaf_rn(e, kInv448, q0);
+    return amax == 0.0f ? 1.0f : (amax <= 3.402823466e38f ? s : amax);
 }
 
 // x / s correctly rounded, for the quotients of the blockwise quantizers:
@@ -86,11 +99,22 @@ __device__ __forceinline__ Divider make_divider(float s) {
     return d;
 }
 
-__device__ __forceinline__ float quotient(const Divider& d, float x) {
-    if (!d.fast) return __fdiv_rn(x, d.s);
-    const float q0 = __fmul_rn(x, d.r);
-    const float e = __fmaf_rn(-d.s, q0, x);
-    return copysignf(__fmaf_rn(e, d.r, q0), x);
+// Two such quotients at once with packed fp32x2 arithmetic (each half
+// rounded as above); d.fast must hold.
+__device__ __forceinline__ void quotient2_fast(const Divider& d, float x0, float x1, float& q0, float& q1) {
+    uint64_t xs, q;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(xs) : "f"(x0), "f"(x1));
+    asm("{\n\t.reg .b64 r2, s2, p, e;\n\t"
+        "mov.b64 r2, {%2, %2};\n\tmov.b64 s2, {%3, %3};\n\t"
+        "mul.rn.f32x2 p, %1, r2;\n\t"
+        "fma.rn.f32x2 e, s2, p, %1;\n\t"
+        "fma.rn.f32x2 %0, e, r2, p;\n\t}\n"
+        : "=l"(q)
+        : "l"(xs), "f"(d.r), "f"(-d.s));
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(q));
+    q0 = copysignf(a, x0);
+    q1 = copysignf(b, x1);
 }
 
 // MX shared exponent e = clamp(floor(log2 amax) - 8, -127, 127) from the fp32

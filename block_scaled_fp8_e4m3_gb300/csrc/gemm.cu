@@ -462,23 +462,29 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                     asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(64) : "memory");
                     a = fmaxf(a, bws->amax_xch[h ^ 1][rl]);
                     asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(64) : "memory");
-                    const float sc = group_scale(a);
+                    const float sc = group_scale_bf16(a);  // D was rounded to bf16
                     const Divider dv = make_divider(sc);
                     if (valid) {
                         uint8_t* codes = p.q_codes + (size_t)m * p.N + ncol0;
                         uint32_t cw[kBwCols / 4];
 #pragma unroll
                         for (int i = 0; i < kBwCols / 8; ++i) {
-                            float f[8];
+                            float f[8], qv[8];
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
                                 f[2 * k] = bf16_lo(packed[4 * i + k]);
                                 f[2 * k + 1] = bf16_hi(packed[4 * i + k]);
                             }
-                            cw[2 * i] = e4m3x2(quotient(dv, f[0]), quotient(dv, f[1])) |
-                                        (e4m3x2(quotient(dv, f[2]), quotient(dv, f[3])) << 16);
-                            cw[2 * i + 1] = e4m3x2(quotient(dv, f[4]), quotient(dv, f[5])) |
-                                            (e4m3x2(quotient(dv, f[6]), quotient(dv, f[7])) << 16);
+                            if (dv.fast) {
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    quotient2_fast(dv, f[2 * k], f[2 * k + 1], qv[2 * k], qv[2 * k + 1]);
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) qv[k] = __fdiv_rn(f[k], dv.s);
+                            }
+                            cw[2 * i] = e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
+                            cw[2 * i + 1] = e4m3x2(qv[4], qv[5]) | (e4m3x2(qv[6], qv[7]) << 16);
                         }
                         if (p.q_v8) {
 #pragma unroll

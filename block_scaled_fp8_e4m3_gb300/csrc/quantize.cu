@@ -42,9 +42,17 @@ __device__ __forceinline__ float amax8(const float (&f)[8]) {
 
 // 8 values divided by s (the IEEE fp32 quotient) and encoded: 8 codes in two words.
 __device__ __forceinline__ uint2 encode8_div(const float (&f)[8], const Divider& d) {
+    float q[8];
+    if (d.fast) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) quotient2_fast(d, f[2 * k], f[2 * k + 1], q[2 * k], q[2 * k + 1]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = __fdiv_rn(f[k], d.s);
+    }
     uint2 r;
-    r.x = e4m3x2(quotient(d, f[0]), quotient(d, f[1])) | (e4m3x2(quotient(d, f[2]), quotient(d, f[3])) << 16);
-    r.y = e4m3x2(quotient(d, f[4]), quotient(d, f[5])) | (e4m3x2(quotient(d, f[6]), quotient(d, f[7])) << 16);
+    r.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
+    r.y = e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16);
     return r;
 }
 
@@ -56,45 +64,69 @@ __device__ __forceinline__ uint2 encode8_mul(const float (&f)[8], float m) {
 }
 
 // ---------------------------------------------------------------------------
-// 1x128 groups along K.  Block = 256 threads = 16 rows (a half-warp per row,
-// 8 bf16 per lane) x 4 consecutive groups; the four 16-byte loads of a
-// thread are issued before any arithmetic.
+// 1x128 groups along K.  Block = 256 threads = 32 rows x 4 consecutive
+// groups; eight lanes share a row's group, each holding 16 of its bf16 values
+// (elements 8*sub.. and 64 + 8*sub.., so that every 16-byte load instruction
+// covers whole 128-byte lines).  All eight loads of a thread are issued before
+// any arithmetic; the per-group work (maximum over 8 lanes, scale, reciprocal)
+// is spread over 16 values per lane.
 // ---------------------------------------------------------------------------
 constexpr int kGK_Groups = 4;
+constexpr int kGK_Rows = 32;
 
-__global__ void __launch_bounds__(256) k_quant_group_k(const uint16_t* __restrict__ x, int64_t M, int64_t K,
-                                                       int64_t ld, uint8_t* __restrict__ codes,
-                                                       float* __restrict__ scales) {
-    const int64_t G = K / 128;
-    const int64_t gchunks = (G + kGK_Groups - 1) / kGK_Groups;
-    const int64_t strip = (int64_t)blockIdx.x / gchunks;
-    const int64_t g0 = ((int64_t)blockIdx.x % gchunks) * kGK_Groups;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int sub = lane & 15;
-    const int64_t row = strip * 16 + warp * 2 + (lane >> 4);
-    const bool row_ok = row < M;
-
-    uint4 v[kGK_Groups];
+// 16 values of one group of one lane: two 8-value halves, encoded into two
+// 8-byte code words.
+__device__ __forceinline__ void encode16(const uint4 (&v)[2], const Divider& d, uint2 (&c)[2]) {
 #pragma unroll
-    for (int u = 0; u < kGK_Groups; ++u) {
-        const int64_t g = g0 + u;
-        v[u] = (row_ok && g < G) ? ld_stream_v4(x + row * ld + g * 128 + sub * 8) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < kGK_Groups; ++u) {
-        const int64_t g = g0 + u;
+    for (int h = 0; h < 2; ++h) {
         float f[8];
-        unpack8(v[u], f);
-        float a = amax8(f);
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+        unpack8(v[h], f);
+        c[h] = encode8_div(f, d);
+    }
+}
+
+__global__ void __launch_bounds__(256, 4) k_quant_group_k(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                          int64_t ld, uint8_t* __restrict__ codes,
+                                                          float* __restrict__ scales) {
+    const int G = (int)(K / 128);
+    const int gchunks = (G + kGK_Groups - 1) / kGK_Groups;
+    const int strip = (int)(blockIdx.x / (unsigned)gchunks);
+    const int g0 = (int)(blockIdx.x - (unsigned)strip * gchunks) * kGK_Groups;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane & 7;
+    const int64_t row = (int64_t)strip * kGK_Rows + warp * 4 + (lane >> 3);
+    const bool row_ok = row < M;
+    const uint16_t* xr = x + row * ld + sub * 8;
+
+    uint4 v[kGK_Groups][2];
+#pragma unroll
+    for (int u = 0; u < kGK_Groups; ++u) {
+        const bool ok = row_ok && g0 + u < G;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            v[u][h] = ok ? ld_stream_v4(xr + (g0 + u) * 128 + h * 64) : make_uint4(0, 0, 0, 0);
+    }
+    uint8_t* cr = codes + row * K + sub * 8;
+#pragma unroll
+    for (int u = 0; u < kGK_Groups; ++u) {
+        const int g = g0 + u;
+        float a = 0.0f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float f[8];
+            unpack8(v[u][h], f);
+            a = fmaxf(a, amax8(f));
+        }
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        const float s = group_scale(a);
+        const float sc = group_scale_bf16(a);
+        uint2 c[2];
+        encode16(v[u], make_divider(sc), c);
         if (row_ok && g < G) {
-            const uint2 c = encode8_div(f, make_divider(s));
-            *reinterpret_cast<uint2*>(codes + row * K + g * 128 + sub * 8) = c;
-            if (sub == 0) scales[g * M + row] = s;
+            *reinterpret_cast<uint2*>(cr + g * 128) = c[0];
+            *reinterpret_cast<uint2*>(cr + g * 128 + 64) = c[1];
+            if (sub == 0) scales[(int64_t)g * M + row] = sc;
         }
     }
 }
@@ -111,7 +143,7 @@ __global__ void __launch_bounds__(256) k_quant_group_m(const uint16_t* __restric
                                                        int64_t ld, uint8_t* __restrict__ codes_t,
                                                        float* __restrict__ scales) {
     __shared__ float red[8][64];
-    __shared__ float col_scale[64];
+    __shared__ float col_scale[64], col_rcp[64];
     __shared__ uint32_t tile[64 * 33];
 
     const int64_t ctiles = (K + 63) / 64;
@@ -147,18 +179,26 @@ __global__ void __launch_bounds__(256) k_quant_group_m(const uint16_t* __restric
         float a = red[0][t];
 #pragma unroll
         for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w][t]);
-        const float s = group_scale(a);
+        const float s = group_scale_bf16(a);
         col_scale[t] = s;
+        col_rcp[t] = __frcp_rn(s);
         if (c0 + t < K) scales[mb * K + c0 + t] = s;
     }
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const float s = col_scale[chunk * 8 + j];
-        const Divider dv = make_divider(s);
+        Divider dv;
+        dv.s = col_scale[chunk * 8 + j];
+        dv.r = col_rcp[chunk * 8 + j];
+        dv.fast = dv.s >= 0x1p-100f && dv.s <= 3.402823466e38f;
         float q[4];
+        if (dv.fast) {
+            quotient2_fast(dv, f[0][j], f[1][j], q[0], q[1]);
+            quotient2_fast(dv, f[2][j], f[3][j], q[2], q[3]);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) q[i] = quotient(dv, f[i][j]);
+            for (int i = 0; i < 4; ++i) q[i] = __fdiv_rn(f[i][j], dv.s);
+        }
         tile[(chunk * 8 + j) * 33 + quad] = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
     }
     __syncthreads();
@@ -216,7 +256,7 @@ __global__ void __launch_bounds__(256) k_quant_block(const uint16_t* __restrict_
     a = red[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) a = fmaxf(a, red[i]);
-    const float s = group_scale(a);
+    const float s = group_scale_bf16(a);
     if (t == 0) {
         scales[nb * KB + kb] = s;
         if (scales_t) scales_t[kb * NB + nb] = s;
@@ -350,7 +390,7 @@ cudaError_t launch_quant_group_k(const uint16_t* x, int64_t M, int64_t K, int64_
                                  float* scales, cudaStream_t st) {
     if (M == 0) return cudaSuccess;
     const int64_t G = K / 128;
-    const int64_t blocks = ((M + 15) / 16) * ((G + kGK_Groups - 1) / kGK_Groups);
+    const int64_t blocks = ((M + kGK_Rows - 1) / kGK_Rows) * ((G + kGK_Groups - 1) / kGK_Groups);
     k_quant_group_k<<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ld, codes, scales);
     return cudaGetLastError();
 }

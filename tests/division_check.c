@@ -1,6 +1,7 @@
-/* Exhaustive host check of the quotient the blockwise quantizers use in place
- * of an IEEE division (Markstein's FMA correction, see make_divider in the
- * CUDA sources).  For every bf16 x and every positive finite bf16 group
+/* Exhaustive host check of the quotients the blockwise quantizers use in
+ * place of IEEE divisions (Markstein's FMA correction, see group_scale_bf16
+ * and make_divider in the CUDA sources).  First, s = RN(a / 448) for every
+ * positive finite bf16 a, from a * RN(1/448) and one correction.  For every bf16 x and every positive finite bf16 group
  * maximum a >= |x|, with s = RN(a / 448) >= 2^-100:
  *   r = RN(1 / s), q0 = RN(x r), e = fma(-s, q0, x), q1 = copysign(fma(e, r, q0), x)
  * must give the same E4M3 code as the IEEE quotient RN(x / s).  The E4M3
@@ -47,6 +48,16 @@ static int e4m3_code(float q) {
 }
 
 int main(void) {
+    /* the scale itself: RN(a / 448) by the same correction of a * RN(1/448) */
+    long long scale_diffs = 0;
+    const float inv448 = 1.0f / 448.0f;
+    for (int ah = 1; ah < 0x7f80; ++ah) {
+        const float a = from_bf16((uint16_t)ah);
+        const float q0 = a * inv448;
+        const float e = fmaf(-448.0f, q0, a);
+        const float sm = fmaf(e, inv448, q0);
+        if (bits_of(sm) != bits_of(a / 448.0f)) scale_diffs++;
+    }
     long long pairs = 0, quotient_diffs = 0, code_diffs = 0, slow_groups = 0;
 #pragma omp parallel for schedule(dynamic, 64) reduction(+ : pairs, quotient_diffs, code_diffs, slow_groups)
     for (int ah = 1; ah < 0x7f80; ++ah) {
@@ -71,7 +82,7 @@ int main(void) {
             }
         }
     }
-    printf("pairs %lld quotient_diffs %lld code_diffs %lld slow_groups %lld\n", pairs, quotient_diffs, code_diffs,
-           slow_groups);
-    return code_diffs != 0;
+    printf("scale_diffs %lld pairs %lld quotient_diffs %lld code_diffs %lld slow_groups %lld\n", scale_diffs, pairs,
+           quotient_diffs, code_diffs, slow_groups);
+    return code_diffs != 0 || scale_diffs != 0;
 }

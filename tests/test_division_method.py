@@ -2,8 +2,9 @@
 
 The blockwise quantizers encode the fp32 quotient x / s (s = amax / 448, the
 "AIS: Adaptive Importance Sampling for Quantized RL" explainer, equation
-Q(X)).  The CUDA kernels form it with one FMA correction of x * RN(1/s)
-(Markstein's method) when s >= 2^-100.  This test compiles a host restatement
+Q(X)).  The CUDA kernels form s from amax * RN(1/448), and x / s from
+x * RN(1/s), each with one FMA correction (Markstein's method; the latter
+when s >= 2^-100).  This test compiles a host restatement
 of that formula and checks it against the IEEE quotient over every bf16 input
 and every bf16 group maximum: the E4M3 codes must agree everywhere.
 """
@@ -18,7 +19,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
-def test_fma_corrected_quotient_matches_ieee_codes_exhaustively():
+def test_fma_corrected_quotients_match_ieee_exhaustively():
     with tempfile.TemporaryDirectory() as tmp:
         exe = os.path.join(tmp, "division_check")
         subprocess.run(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-o", exe,
@@ -26,5 +27,6 @@ def test_fma_corrected_quotient_matches_ieee_codes_exhaustively():
         out = subprocess.run([exe], capture_output=True, text=True, timeout=900)
     fields = dict(zip(out.stdout.split()[0::2], map(int, out.stdout.split()[1::2])))
     assert out.returncode == 0, out.stdout
+    assert fields["scale_diffs"] == 0
     assert fields["code_diffs"] == 0
     assert fields["pairs"] > 10**9  # every (x, group maximum) pair with s >= 2^-100
