@@ -131,6 +131,26 @@ def time_kernel(fn, flush, reps, warmup=3):
     return float(np.mean([a.elapsed_time(b) for a, b in ts]))
 
 
+def gemm_traffic():
+    """DRAM bytes (read + write) per launch of the step's GEMM, from the
+    committed ncu summary, or None when the kernel source has changed since
+    those counters were taken (the summary records the sha256 of gemm.cu)."""
+    import hashlib
+    here = os.path.dirname(os.path.abspath(__file__))
+    summary = os.path.join(here, "profiles", "k_gemm_blockwise_fused_mlp_8192x4096x12288.md")
+    src = os.path.join(here, "block_scaled_fp8_e4m3_gb300", "csrc", "gemm.cu")
+    try:
+        text = open(summary).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(("traffic_bytes_per_launch:",
+                                                                                       "gemm_cu_sha256:")))
+    if fields.get("gemm_cu_sha256", "").strip() != digest or "traffic_bytes_per_launch" not in fields:
+        return None
+    return int(fields["traffic_bytes_per_launch"].strip())
+
+
 # ------------------------------------------------------------------ our arm
 def make_step(fp8, X, W, dev):
     qx = fp8.quantize_group(X, "K")
@@ -477,7 +497,7 @@ def main():
                 "achieved": round(gemm_tf, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                 "frac": round(gemm_tf / fp8_peak, 4),
                 "peak_basis": f"2 x {pk['source']} bf16 burst {pk['bf16_tflops']} TFLOP/s (FP8:BF16 = 2:1)",
-                "traffic": None}
+                "traffic": gemm_traffic()}
     qx_gbs = M * K * (3 + 4 / 128) / (per_kernel[0] * 1e-3) / 1e9
     qw_gbs = N * K * (3 + 4 / 16384) / (per_kernel[1] * 1e-3) / 1e9
     step_kernels = {
@@ -535,7 +555,8 @@ def main():
                 "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
                 "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "seed": 2,
                            "step": "quant X 1x128, quant W 128x128, GEMM+fused quant of Y, sync pack W, install W",
-                           "l2": "flushed between steps (256 MB write)", "parallelism": f"replicas x{world}"},
+                           "l2": "flushed between steps (256 MB write, then 256 MB read)",
+                           "parallelism": f"replicas x{world}"},
                 "roofline": roofline, "step_kernels": step_kernels, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clocks, "peaks": pk,
                 "kernels": kernels}
