@@ -529,6 +529,7 @@ struct MxParams {
     uint8_t* q_scales;
     StatusBlock* st;
     int tiles_n;
+    int d_v8;  // D rows allow 32-byte stores
 };
 
 struct TileCoord {
@@ -729,11 +730,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t m = (int64_t)c.row0 + rl;
             if (mvalid && hvalid) {
                 uint16_t* d = p.D + m * p.ldd + ncol0;
+                if (p.d_v8) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (ncol0 + 8 * i < p.N)
-                        reinterpret_cast<uint4*>(d)[i] =
-                            make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                    for (int i = 0; i < 8; ++i)
+                        if (ncol0 + 16 * i < p.N) st_v8(d + 16 * i, packed + 8 * i);  // N % 16 == 0
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (ncol0 + 8 * i < p.N)
+                            reinterpret_cast<uint4*>(d)[i] =
+                                make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                }
                 if (p.q_codes != nullptr) {
                     const uint32_t sc = quant_row_mx(packed, p.q_codes + m * p.N + ncol0);
                     *reinterpret_cast<uint32_t*>(p.q_scales + mx_scale_offset(m, ncol0 / 32, q_atoms_k)) = sc;
@@ -867,6 +874,7 @@ cudaError_t launch_gemm_mx(const GemmMxArgs& a, StatusBlock* status, cudaStream_
     p.q_scales = a.q_scales;
     p.st = status;
     p.tiles_n = (int)((a.N + kMxBN - 1) / kMxBN);
+    p.d_v8 = (reinterpret_cast<uintptr_t>(a.D) % 32 == 0) && ((a.ldd * 2) % 32 == 0);
     // upper bound of the tile count (the exact count depends on device-side offsets)
     const int64_t mtiles = a.m_offsets ? (a.M + BM - 1) / BM + a.G : (a.M + BM - 1) / BM;
     const int64_t tiles = mtiles * p.tiles_n;
