@@ -319,6 +319,25 @@ __device__ __forceinline__ void tc_mma_f8f6f4_pair(uint32_t d_tmem, uint64_t ade
         : "memory");
 }
 
+// block-scaled MX MMA on a CTA pair; each CTA's tensor core applies the
+// scale factors in its own TMEM (its A rows' scales, all N columns' B scales)
+__device__ __forceinline__ void tc_mma_mxf8f6f4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                     uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}\n" ::
+            "r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+// shared -> TMEM copy on a CTA pair: each CTA copies from its own shared
+// memory (same address) into its own TMEM
+__device__ __forceinline__ void tc_cp_pair_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // arrive on the barrier at the same offset in every CTA of cta_mask once the
 // pair MMAs issued so far by this thread have completed
 __device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask) {

@@ -68,11 +68,14 @@ constexpr int kBwCols = kBwBN / (kBwEpiWarps / 4);       // 64 columns per epilo
 constexpr uint32_t kIdescBlockwise = idesc_f8f6f4(2 * BM, 128);
 
 // MX kernel
+// CTA pairs compute 256x256 tiles (tcgen05.mma.cta_group::2, M=256, N=256):
+// each CTA stages its 128 rows of A, its 128 of the tile's 256 rows of B, the
+// scale atom of its A rows and both scale atoms of the tile's B rows.
 constexpr int kMxBN = 256;
-constexpr int kMxStages = 4;
-constexpr uint32_t kMxStageBytes = (BM + kMxBN) * BK;  // 48 KB
-constexpr uint32_t kSfStageBytes = 1536;                // SFA atom + two SFB atoms
-constexpr uint32_t kMxTmemCols = 512;                   // accumulator 256 + scale factors
+constexpr int kMxStages = 6;
+constexpr uint32_t kMxStageBytes = (BM + kMxBN / 2) * BK;  // 32 KB
+constexpr uint32_t kSfStageBytes = 1536;                    // SFA atom + two SFB atoms
+constexpr uint32_t kMxTmemCols = 512;                       // accumulator 256 + scale factors
 
 struct alignas(16) Barriers {
     uint64_t full[kMaxStages];
@@ -82,7 +85,7 @@ struct alignas(16) Barriers {
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-    int num_mtiles;  // MX: total 128-row tiles over all groups
+    int num_mtiles;  // MX: total 256-row cluster tiles over all groups
 };
 
 // blockwise kernel only (16-byte aligned: float4 reads and 16-byte cp.async)
@@ -99,7 +102,7 @@ constexpr size_t kSmemBlockwise = 1024 + (size_t)kBwStages * kBwStageBytes + siz
 static_assert(sizeof(Barriers) % 16 == 0, "BwShared must start 16-byte aligned");
 static_assert(kSmemBlockwise <= 232448, "blockwise shared memory over the 227 KB limit");
 constexpr size_t kSmemMx = 1024 + (size_t)kMxStages * (kMxStageBytes + kSfStageBytes) + sizeof(Barriers) +
-                           2 * (kMaxGroups + 1) * sizeof(int);
+                           3 * (kMaxGroups + 1) * sizeof(int);
 static_assert(kSmemMx <= 232448, "MX shared memory over the 227 KB limit");
 
 __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
@@ -533,45 +536,60 @@ struct MxParams {
 };
 
 struct TileCoord {
-    int g, mt_global, row0, rows, tn;  // rows = valid rows of the group in this tile
+    int g;          // group
+    int mt;         // this CTA's 128-row tile within the group
+    int atom_row;   // its row of scale atoms (clamped into the group)
+    int row0, rows;  // first row of the tile; valid rows of the group in it (0..128)
+    int tn;
 };
 
-__device__ __forceinline__ TileCoord mx_tile(int tile, int tiles_n, const int* pfx, const int* offs, int G) {
+// Cluster tile -> (group, 256-row cluster tile, 256-column tile) by binary
+// search over the prefix of cluster tiles per group; then this CTA's half.
+__device__ __forceinline__ TileCoord mx_tile(int tile, int tiles_n, const int* pfx, const int* pfx2, const int* offs,
+                                            int G, uint32_t rank) {
     TileCoord c;
-    c.mt_global = tile / tiles_n;
-    c.tn = tile % tiles_n;
-    int lo = 0, hi = G;  // largest g with pfx[g] <= mt_global
+    const int mt2_global = tile / tiles_n;
+    c.tn = tile - mt2_global * tiles_n;
+    int lo = 0, hi = G;  // largest g with pfx2[g] <= mt2_global
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (pfx[mid] <= c.mt_global) lo = mid; else hi = mid;
+        if (pfx2[mid] <= mt2_global) lo = mid; else hi = mid;
     }
     c.g = lo;
-    const int mt = c.mt_global - pfx[lo];
-    c.row0 = offs[lo] + mt * BM;
+    c.mt = 2 * (mt2_global - pfx2[lo]) + (int)rank;
+    const int ntiles = pfx[lo + 1] - pfx[lo];  // 128-row tiles of the group (>= 1 here)
+    c.atom_row = pfx[lo] + (c.mt < ntiles ? c.mt : ntiles - 1);
+    c.row0 = offs[lo] + c.mt * BM;
     const int left = offs[lo + 1] - c.row0;
-    c.rows = left < BM ? left : BM;
+    c.rows = left < 0 ? 0 : (left < BM ? left : BM);
     return c;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const MxParams p) {
+    k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB, const MxParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = aligned_smem(smem_raw);
     uint8_t* sf = smem + kMxStages * kMxStageBytes;
     Barriers* bar = reinterpret_cast<Barriers*>(sf + kMxStages * kSfStageBytes);
     int* offs = reinterpret_cast<int*>(bar + 1);  // [G+1] row offsets
     int* pfx = offs + (kMaxGroups + 1);           // [G+1] prefix of 128-row tiles (= scale atom rows)
+    int* pfx2 = pfx + (kMaxGroups + 1);           // [G+1] prefix of 256-row cluster tiles
     volatile int* abort = &bar->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G;
+    const uint32_t rank = cluster_ctarank();  // 0: leader CTA (issues the MMAs)
+    const int cid = (int)(blockIdx.x >> 1), ncl = (int)(gridDim.x >> 1);
 
     if (threadIdx.x == 0) {
+        // full[s], acc_empty (leader only): the leader producer's expect_tx
+        // arrival for both CTAs' bytes; one arrival per epilogue warp of both CTAs
         for (int s = 0; s < kMxStages; ++s) {
             mbar_init(&bar->full[s], 1);
             mbar_init(&bar->empty[s], 1);
         }
         mbar_init(&bar->acc_full[0], 1);
-        mbar_init(&bar->acc_empty[0], kEpiThreads / 32);
+        mbar_init(&bar->acc_empty[0], 2 * (kEpiThreads / 32));
         mbar_init(&bar->drain, 1);
         bar->abort = 0;
         fence_mbar_init();
@@ -579,11 +597,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmSFA);
+        prefetch_tensormap(&tmSFB);
     }
-    if (warp == 1) tmem_alloc(&bar->tmem_base, kMxTmemCols);
+    if (warp == 1) tmem_alloc_pair(&bar->tmem_base, kMxTmemCols);
     if (warp == 2) {
-        // group row offsets and the prefix sum of their 128-row tile counts
-        int carry = 0;
+        // group row offsets and the prefix sums of their 128- and 256-row tile counts
+        int carry = 0, carry2 = 0;
         for (int base = 0; base < G; base += 32) {
             const int g = base + lane;
             int o0 = 0, o1 = 0;
@@ -594,41 +614,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             int cnt = (g < G) ? (o1 - o0 + BM - 1) / BM : 0;
             if (cnt < 0) cnt = 0;
-            int incl = cnt;
+            const int cnt2 = (cnt + 1) / 2;
+            int incl = cnt, incl2 = cnt2;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
+                const int v2 = __shfl_up_sync(0xffffffffu, incl2, o);
+                if (lane >= o) {
+                    incl += v;
+                    incl2 += v2;
+                }
             }
-            if (g < G) pfx[g] = carry + incl - cnt;
+            if (g < G) {
+                pfx[g] = carry + incl - cnt;
+                pfx2[g] = carry2 + incl2 - cnt2;
+            }
             carry += __shfl_sync(0xffffffffu, incl, 31);
+            carry2 += __shfl_sync(0xffffffffu, incl2, 31);
         }
         if (lane == 0) {
             pfx[G] = carry;
+            pfx2[G] = carry2;
             offs[G] = p.m_offsets ? p.m_offsets[G] : p.M;
-            bar->num_mtiles = carry;
+            bar->num_mtiles = carry2;
         }
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // barriers, group tables and TMEM ready in both CTAs
     tc_fence_after();
     const uint32_t tmem = bar->tmem_base;
     const int KB = p.K / BK;
     const int num_tiles = bar->num_mtiles * p.tiles_n;
     const uint32_t sf_col0 = 256;  // TMEM columns [256, 256 + 16*kMxStages): scale factors
+    const uint32_t full_leader = mapa_shared(&bar->full[0], 0);
+    const uint32_t acc_empty_leader = mapa_shared(&bar->acc_empty[0], 0);
 
     if (warp == 0) {
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
-            uint32_t fills[kMxStages] = {0, 0, 0, 0};
             bool ok = true;
-            const int64_t atoms_k = p.K / 128;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                const TileCoord c = mx_tile(tile, p.tiles_n, pfx, offs, G);
-                const int brow0 = c.g * p.N + c.tn * kMxBN;
-                const bool two_b_atoms = c.tn * kMxBN + 128 < p.N;
-                const uint32_t bytes = kMxStageBytes + 512u + (two_b_atoms ? 1024u : 512u);
+            const int atoms_k = p.K / 128;
+            const int b_atom_rows = (p.G * p.N + 127) / 128;
+            for (int tile = cid; tile < num_tiles && ok; tile += ncl) {
+                const TileCoord c = mx_tile(tile, p.tiles_n, pfx, pfx2, offs, G, rank);
+                const int bcol0 = c.g * p.N + c.tn * kMxBN;        // first B row of the tile
+                const int batom0 = bcol0 / 128;                      // its scale atom row
+                const int batom1 = c.tn * kMxBN + 128 < p.N && batom0 + 1 < b_atom_rows ? batom0 + 1 : batom0;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait_bounded(&bar->empty[s], ph ^ 1, abort, p.st, 11)) {
                         ok = false;
@@ -636,31 +668,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     uint8_t* stage = smem + s * kMxStageBytes;
                     uint8_t* sfs = sf + s * kSfStageBytes;
-                    mbar_arrive_expect_tx(&bar->full[s], bytes);
-                    tma_load_2d(stage, &tmA, &bar->full[s], kb * BK, c.row0);
-                    tma_load_2d(stage + BM * BK, &tmB, &bar->full[s], kb * BK, brow0);
-                    bulk_load(sfs, p.sfa + ((int64_t)c.mt_global * atoms_k + kb) * 512, 512, &bar->full[s]);
-                    bulk_load(sfs + 512, p.sfb + ((int64_t)(brow0 / 128) * atoms_k + kb) * 512, 512, &bar->full[s]);
-                    if (two_b_atoms)
-                        bulk_load(sfs + 1024, p.sfb + ((int64_t)(brow0 / 128 + 1) * atoms_k + kb) * 512, 512,
-                                  &bar->full[s]);
-                    ++fills[s];
+                    if (rank == 0) mbar_arrive_expect_tx(&bar->full[s], 2 * (kMxStageBytes + kSfStageBytes));
+                    const uint32_t fb = full_leader + 8u * (uint32_t)s;
+                    tma_load_2d_pair(stage, &tmA, fb, kb * BK, c.row0);
+                    tma_load_2d_pair(stage + BM * BK, &tmB, fb, kb * BK, bcol0 + 128 * (int)rank);
+                    // scale atoms as 2 x 256-byte rows of the [atoms * 2][256] byte views
+                    tma_load_2d_pair(sfs, &tmSFA, fb, 0, 2 * (c.atom_row * atoms_k + kb));
+                    tma_load_2d_pair(sfs + 512, &tmSFB, fb, 0, 2 * (batom0 * atoms_k + kb));
+                    tma_load_2d_pair(sfs + 1024, &tmSFB, fb, 0, 2 * (batom1 * atoms_k + kb));
                     if (++s == kMxStages) {
                         s = 0;
                         ph ^= 1;
                     }
                 }
             }
-            if (!ok)
-                for (int i = 0; i < kMxStages; ++i)
-                    if (fills[i]) mbar_wait_drain(&bar->full[i], (fills[i] - 1) & 1, p.st);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             int s = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            for (int tile = cid; tile < num_tiles && ok; tile += ncl) {
                 if (!mbar_wait_bounded(&bar->acc_empty[0], aph ^ 1, abort, p.st, 12)) break;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait_bounded(&bar->full[s], ph, abort, p.st, 13)) {
@@ -672,26 +700,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sf_addr = smem_u32(sf + s * kSfStageBytes);
                     const uint32_t tsfa = tmem + sf_col0 + 16u * s;
                     const uint32_t tsfb = tsfa + 4;
-                    tc_cp_32x128b_warpx4(tsfa, sdesc_sf_32x16(sf_addr));
-                    tc_cp_32x128b_warpx4(tsfb, sdesc_sf_32x16(sf_addr + 512));
-                    tc_cp_32x128b_warpx4(tsfb + 4, sdesc_sf_32x16(sf_addr + 1024));
+                    // each CTA copies its own shared-memory scales into its own TMEM
+                    tc_cp_pair_32x128b_warpx4(tsfa, sdesc_sf_32x16(sf_addr));
+                    tc_cp_pair_32x128b_warpx4(tsfb, sdesc_sf_32x16(sf_addr + 512));
+                    tc_cp_pair_32x128b_warpx4(tsfb + 4, sdesc_sf_32x16(sf_addr + 1024));
                     const uint64_t adesc = sdesc_k_sw128(a_addr);
                     const uint64_t bdesc = sdesc_k_sw128(a_addr + BM * BK);
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k)
-                        tc_mma_mxf8f6f4(tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8f6f4(BM, kMxBN, k, k), tsfa, tsfb,
-                                        (kb > 0 || k > 0) ? 1u : 0u);
-                    tc_commit(&bar->empty[s]);
+                        tc_mma_mxf8f6f4_pair(tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8f6f4(2 * BM, kMxBN, k, k),
+                                             tsfa, tsfb, (kb > 0 || k > 0) ? 1u : 0u);
+                    tc_commit_pair(&bar->empty[s], 3);
                     if (++s == kMxStages) {
                         s = 0;
                         ph ^= 1;
                     }
                 }
                 if (!ok) break;
-                tc_commit(&bar->acc_full[0]);
+                tc_commit_pair(&bar->acc_full[0], 3);
                 aph ^= 1;
             }
-            tc_commit(&bar->drain);
+            tc_commit_pair(&bar->drain, 1);
             mbar_wait_drain(&bar->drain, 0, p.st);
         }
     } else if (warp >= kEpiWarp0) {
@@ -699,8 +728,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
         const int64_t q_atoms_k = (p.N + 127) / 128;
         uint32_t aph = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const TileCoord c = mx_tile(tile, p.tiles_n, pfx, offs, G);
+        for (int tile = cid; tile < num_tiles; tile += ncl) {
+            const TileCoord c = mx_tile(tile, p.tiles_n, pfx, pfx2, offs, G, rank);
             const int rl = 32 * q + lane;
             const int ncol0 = c.tn * kMxBN + 128 * h;
             const bool mvalid = rl < c.rows, hvalid = ncol0 < p.N;
@@ -723,9 +752,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
                 }
             }
+            // the accumulator is read: hand it back to the leader's MMA thread
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->acc_empty[0]);
+            if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
             aph ^= 1;
             const int64_t m = (int64_t)c.row0 + rl;
             if (mvalid && hvalid) {
@@ -752,12 +782,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    // neither CTA leaves while the other may still signal its barriers or
+    // the leader's MMAs may still write its TMEM
+    __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, kMxTmemCols);
+        tmem_dealloc_pair(tmem, kMxTmemCols);
     }
 }
 
@@ -786,6 +819,19 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, 
     cuuint32_t es[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D u8 tensor map, no swizzle, over a row-major [rows][cols] byte array.
+bool make_map_plain_u8(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {(cuuint32_t)cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -856,9 +902,15 @@ cudaError_t launch_gemm_blockwise(const GemmBlockwiseArgs& a, StatusBlock* statu
 
 cudaError_t launch_gemm_mx(const GemmMxArgs& a, StatusBlock* status, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
-    CUtensorMap tmA, tmB;
+    // scale buffers: per-group padded atom rows (grouped) or ceil(M/128) atom rows
+    const int64_t atoms_k = a.K / 128;
+    const int64_t a_atom_rows = a.m_offsets ? (a.M + BM - 1) / BM + a.G : (a.M + BM - 1) / BM;
+    const int64_t b_atom_rows = (a.N * a.G + 127) / 128;
+    CUtensorMap tmA, tmB, tmSFA, tmSFB;
     if (!make_map(&tmA, a.a_codes, (uint64_t)a.K, (uint64_t)a.M, BM) ||
-        !make_map(&tmB, a.b_codes, (uint64_t)a.K, (uint64_t)a.N * (uint64_t)a.G, kMxBN))
+        !make_map(&tmB, a.b_codes, (uint64_t)a.K, (uint64_t)a.N * (uint64_t)a.G, kMxBN / 2) ||
+        !make_map_plain_u8(&tmSFA, a.sfa, 256, (uint64_t)(2 * a_atom_rows * atoms_k), 2) ||
+        !make_map_plain_u8(&tmSFB, a.sfb, 256, (uint64_t)(2 * b_atom_rows * atoms_k), 2))
         return cudaErrorInvalidValue;
     MxParams p;
     p.sfa = a.sfa;
@@ -875,14 +927,36 @@ cudaError_t launch_gemm_mx(const GemmMxArgs& a, StatusBlock* status, cudaStream_
     p.st = status;
     p.tiles_n = (int)((a.N + kMxBN - 1) / kMxBN);
     p.d_v8 = (reinterpret_cast<uintptr_t>(a.D) % 32 == 0) && ((a.ldd * 2) % 32 == 0);
-    // upper bound of the tile count (the exact count depends on device-side offsets)
-    const int64_t mtiles = a.m_offsets ? (a.M + BM - 1) / BM + a.G : (a.M + BM - 1) / BM;
+    // upper bound of the cluster-tile count (the exact count depends on device-side offsets)
+    const int64_t mtiles = a.m_offsets ? (a.M + 2 * BM - 1) / (2 * BM) + a.G : (a.M + 2 * BM - 1) / (2 * BM);
     const int64_t tiles = mtiles * p.tiles_n;
-    const int grid = tiles < sm_count() ? (int)tiles : sm_count();
     cudaError_t e = cudaFuncSetAttribute(k_gemm_mx, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMx);
     if (e != cudaSuccess) return e;
-    k_gemm_mx<<<grid, kThreads, kSmemMx, st>>>(tmA, tmB, p);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (unsigned)tiles);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemMx;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static int max_pairs[64] = {0};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int& mp = max_pairs[dev & 63];
+    if (mp <= 0) {
+        e = cudaOccupancyMaxActiveClusters(&mp, k_gemm_mx, &cfg);
+        if (e != cudaSuccess) return e;
+        if (mp <= 0) return cudaErrorInvalidConfiguration;
+    }
+    const int64_t pairs = tiles < mp ? tiles : mp;
+    cfg.gridDim = dim3(2 * (unsigned)pairs);
+    return cudaLaunchKernelEx(&cfg, k_gemm_mx, tmA, tmB, tmSFA, tmSFB, p);
 }
 
 }  // namespace fp8bs
