@@ -612,26 +612,35 @@ fp8_status fp8_sync_install(const void* payload_dev, uint64_t bytes, const fp8_s
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const uint8_t* pay = static_cast<const uint8_t*>(payload_dev);
     std::vector<uint8_t> expect = build_table(dst, n, lay, total);
-    std::vector<uint8_t> got(expect.size());
-    cudaError_t e = cudaMemcpyAsync(got.data(), pay, got.size(), cudaMemcpyDeviceToHost, cs);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
-    if (e != cudaSuccess) return cuda_fail(e, "sync_install header read");
-    if (get64(&got[0]) != kSyncMagic || get32(&got[8]) != 1)
-        return fail(FP8_ERR_BAD_PAYLOAD, "not a version-1 FP8 sync payload");
-    if (get32(&got[12]) != (uint32_t)n)
-        return fail(FP8_ERR_BAD_PAYLOAD, "payload has %u entries, %d destinations", get32(&got[12]), n);
-    // every byte of header and table except the checksum must match what
-    // the destinations imply
-    for (size_t i = 0; i < expect.size(); ++i) {
-        if (i >= 32 && i < 40) continue;
-        if (got[i] != expect[i]) {
-            const long long ent = i < kHeaderBytes ? -1 : (long long)((i - kHeaderBytes) / kEntryBytes);
-            return fail(FP8_ERR_BAD_PAYLOAD, "payload header/table byte %zu differs (entry %lld)", i, ent);
+    cudaError_t e;
+    if (expect.size() <= (size_t)kMaxExpectBytes) {
+        // every byte of header and table except the checksum must match what
+        // the destinations imply: checked on the device by the verify kernel
+        // (no host round trip); a mismatch installs nothing and is reported
+        // by fp8_status_poll
+        static thread_local ExpectTable et;
+        et.bytes = (uint32_t)expect.size();
+        memcpy(et.data, expect.data(), expect.size());
+        e = launch_sync_verify(pay, expect.size(), total, table_checksum(expect), st, cs, &et);
+    } else {
+        std::vector<uint8_t> got(expect.size());
+        e = cudaMemcpyAsync(got.data(), pay, got.size(), cudaMemcpyDeviceToHost, cs);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+        if (e != cudaSuccess) return cuda_fail(e, "sync_install header read");
+        if (get64(&got[0]) != kSyncMagic || get32(&got[8]) != 1)
+            return fail(FP8_ERR_BAD_PAYLOAD, "not a version-1 FP8 sync payload");
+        if (get32(&got[12]) != (uint32_t)n)
+            return fail(FP8_ERR_BAD_PAYLOAD, "payload has %u entries, %d destinations", get32(&got[12]), n);
+        for (size_t i = 0; i < expect.size(); ++i) {
+            if (i >= 32 && i < 40) continue;
+            if (got[i] != expect[i]) {
+                const long long ent = i < kHeaderBytes ? -1 : (long long)((i - kHeaderBytes) / kEntryBytes);
+                return fail(FP8_ERR_BAD_PAYLOAD, "payload header/table byte %zu differs (entry %lld)", i, ent);
+            }
         }
+        put64(&got[32], 0);
+        e = launch_sync_verify(pay, expect.size(), total, table_checksum(got), st, cs);
     }
-    put64(&got[32], 0);
-    const unsigned long long table_sum = table_checksum(got);
-    e = launch_sync_verify(pay, expect.size(), total, table_sum, st, cs);
     if (e != cudaSuccess) return cuda_fail(e, "sync_install verify");
     std::vector<CopySeg> segs;
     for (int32_t i = 0; i < n; ++i) {
@@ -662,6 +671,8 @@ fp8_status fp8_status_poll(fp8_stream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "status_poll clear");
     if (bits[0] & kErrTimeout)
         return fail(FP8_ERR_TIMEOUT, "a bounded on-chip wait expired (site %u)", bits[1]);
+    if (bits[0] & kErrBadPayload)
+        return fail(FP8_ERR_BAD_PAYLOAD, "sync payload header/table does not match the destinations; nothing installed");
     if (bits[0] & kErrChecksum) return fail(FP8_ERR_CHECKSUM, "sync payload checksum mismatch; nothing installed");
     return fail(FP8_ERR_INVALID_ARG, "a kernel rejected a device-side argument (e.g. a gather index)");
 }

@@ -21,6 +21,7 @@ enum : unsigned int {
     kErrTimeout = 1u,
     kErrChecksum = 2u,
     kErrDeviceArg = 4u,
+    kErrBadPayload = 8u,
 };
 
 // One per device, allocated on first use; cleared by fp8_status_poll().
@@ -30,7 +31,9 @@ struct StatusBlock {
     unsigned long long sum;      // checksum accumulator of fp8_sync_install
     unsigned int blocks_done;    // blocks of the verify kernel that finished
     unsigned int verdict;        // 0: payload verified, 1: mismatch
-    unsigned long long reserved[4];
+    unsigned int header_bad;     // set by fp8_sync_install's device-side header/table check
+    unsigned int reserved32;
+    unsigned long long reserved[3];
 };
 
 // A bounded wait gives up after this long.  Legitimate waits inside one

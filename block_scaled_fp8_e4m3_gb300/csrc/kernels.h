@@ -66,8 +66,16 @@ struct CopySeg {
     uint64_t dst_word0;  // payload word index of dst[0] (pack: checksum position)
 };
 cudaError_t launch_sync_pack(const CopySeg* segs, int n, unsigned long long* checksum_field, cudaStream_t st);
+// Expected header + entry table of a payload, compared on the device with
+// the payload's own bytes (the checksum field excepted); bytes == 0: none.
+constexpr int kMaxExpectBytes = 64 + 128 * 24;
+struct ExpectTable {
+    uint32_t bytes;
+    uint8_t data[kMaxExpectBytes];
+};
 cudaError_t launch_sync_verify(const uint8_t* payload, uint64_t data_offset, uint64_t total_bytes,
-                               unsigned long long table_sum, StatusBlock* status, cudaStream_t st);
+                               unsigned long long table_sum, StatusBlock* status, cudaStream_t st,
+                               const ExpectTable* expect = nullptr);
 cudaError_t launch_sync_scatter(const CopySeg* segs, int n, const StatusBlock* status, cudaStream_t st);
 
 }  // namespace fp8bs

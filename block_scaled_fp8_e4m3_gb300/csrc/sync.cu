@@ -97,7 +97,15 @@ __global__ void __launch_bounds__(256) k_sync_pack(const SegTable tab, unsigned 
 
 __global__ void __launch_bounds__(256) k_sync_verify(const uint8_t* __restrict__ payload, uint64_t data_offset,
                                                      uint64_t total_bytes, unsigned long long table_sum,
-                                                     StatusBlock* st) {
+                                                     StatusBlock* st, const __grid_constant__ ExpectTable expect) {
+    if (blockIdx.x == 0 && expect.bytes != 0) {
+        // header and entry table against what the destinations imply (the
+        // checksum field, bytes 32..39, is what the data is checked against)
+        bool bad = false;
+        for (uint32_t i = threadIdx.x; i < expect.bytes; i += blockDim.x)
+            if ((i < 32 || i >= 40) && payload[i] != expect.data[i]) bad = true;
+        if (__syncthreads_or(bad) && threadIdx.x == 0) atomicExch(&st->header_bad, 1u);
+    }
     const uint64_t c0 = data_offset / 16, c1 = total_bytes / 16;
     unsigned long long sum = 0;
     for (uint64_t c = c0 + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; c < c1;
@@ -116,9 +124,11 @@ __global__ void __launch_bounds__(256) k_sync_verify(const uint8_t* __restrict__
             __threadfence();
             const unsigned long long total = atomicAdd(&st->sum, 0ull) + table_sum;
             const unsigned long long stored = *reinterpret_cast<const unsigned long long*>(payload + 32);
-            const unsigned int bad = (total != stored) ? 1u : 0u;
+            const unsigned int header_bad = atomicExch(&st->header_bad, 0u);
+            const unsigned int bad = (total != stored || header_bad) ? 1u : 0u;
             st->verdict = bad;
-            if (bad) atomicOr(&st->error_bits, kErrChecksum);
+            if (header_bad) atomicOr(&st->error_bits, kErrBadPayload);
+            else if (bad) atomicOr(&st->error_bits, kErrChecksum);
             st->sum = 0;
             st->blocks_done = 0;
             __threadfence();
@@ -176,9 +186,11 @@ cudaError_t launch_sync_pack(const CopySeg* segs, int n, unsigned long long* che
 }
 
 cudaError_t launch_sync_verify(const uint8_t* payload, uint64_t data_offset, uint64_t total_bytes,
-                               unsigned long long table_sum, StatusBlock* status, cudaStream_t st) {
-    k_sync_verify<<<grid_for((total_bytes - data_offset) / 16), 256, 0, st>>>(payload, data_offset, total_bytes,
-                                                                               table_sum, status);
+                               unsigned long long table_sum, StatusBlock* status, cudaStream_t st,
+                               const ExpectTable* expect) {
+    static const ExpectTable none = {};
+    k_sync_verify<<<grid_for((total_bytes - data_offset) / 16), 256, 0, st>>>(
+        payload, data_offset, total_bytes, table_sum, status, expect ? *expect : none);
     return cudaGetLastError();
 }
 

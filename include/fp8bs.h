@@ -253,11 +253,15 @@ fp8_status fp8_sync_pack(const fp8_sync_entry* entries, int32_t n, void* payload
 
 /* Installs a payload into the destination tensors described by dst (device
  * buffers of the rollout side).  Never quantizes: the bytes are copied.
- * The header and table are read back and checked against dst on the host
- * (this synchronizes `stream`); a mismatch returns FP8_ERR_BAD_PAYLOAD and
- * writes nothing.  The checksum is then verified on the device before any
- * destination byte is written; on mismatch nothing is written and
- * fp8_status_poll() returns FP8_ERR_CHECKSUM. */
+ * Every header and table byte (the checksum field excepted) must equal what
+ * dst implies, and the checksum must match; both are verified on the device
+ * before any destination byte is written.  For up to 24 entries the header
+ * check also runs on the device (the call does not synchronize `stream`): a
+ * mismatch writes nothing and fp8_status_poll() returns FP8_ERR_BAD_PAYLOAD.
+ * With more entries the header and table are read back and checked on the
+ * host (this synchronizes `stream`) and a mismatch is returned at once.  A
+ * checksum mismatch writes nothing and fp8_status_poll() returns
+ * FP8_ERR_CHECKSUM. */
 fp8_status fp8_sync_install(const void* payload_dev, uint64_t bytes, const fp8_sync_entry* dst,
                             int32_t n, fp8_stream_t stream);
 

@@ -92,7 +92,7 @@ def test_corrupted_payload_writes_nothing():
     fp8.sync_install(good, dst)
 
 
-def test_header_mismatch_rejected_on_host():
+def test_header_mismatch_rejected():
     W, X, M, N = _trainer_tensors(seed=20)
     entries = _entries(W, X, M, N)
     payload = fp8.sync_pack(entries)
