@@ -134,19 +134,19 @@ def time_kernel(fn, flush, reps, warmup=3):
 def gemm_traffic():
     """DRAM bytes (read + write) per launch of the step's GEMM, from the
     committed ncu summary, or None when the kernel source has changed since
-    those counters were taken (the summary records the sha256 of gemm.cu)."""
+    those counters were taken (the summary records the sha256 of gemm_blockwise.cu)."""
     import hashlib
     here = os.path.dirname(os.path.abspath(__file__))
     summary = os.path.join(here, "profiles", "k_gemm_blockwise_fused_mlp_8192x4096x12288.md")
-    src = os.path.join(here, "block_scaled_fp8_e4m3_gb300", "csrc", "gemm.cu")
+    src = os.path.join(here, "block_scaled_fp8_e4m3_gb300", "csrc", "gemm_blockwise.cu")
     try:
         text = open(summary).read()
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
     except OSError:
         return None
     fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(("traffic_bytes_per_launch:",
-                                                                                       "gemm_cu_sha256:")))
-    if fields.get("gemm_cu_sha256", "").strip() != digest or "traffic_bytes_per_launch" not in fields:
+                                                                                       "gemm_blockwise_cu_sha256:")))
+    if fields.get("gemm_blockwise_cu_sha256", "").strip() != digest or "traffic_bytes_per_launch" not in fields:
         return None
     return int(fields["traffic_bytes_per_launch"].strip())
 

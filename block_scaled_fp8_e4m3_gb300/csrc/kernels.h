@@ -24,7 +24,7 @@ cudaError_t launch_permute_rows_mx(const uint8_t* src_codes, const uint8_t* src_
                                    int64_t total, uint8_t* dst_codes, uint8_t* dst_scales, int64_t dst_scale_bytes,
                                    StatusBlock* status, cudaStream_t st);
 
-// gemm.cu
+// gemm_blockwise.cu, gemm_mx.cu
 struct GemmBlockwiseArgs {
     const uint8_t* a_codes;  // [M][K]
     const uint8_t* b_codes;  // [N][K]
