@@ -27,9 +27,7 @@ def load():
     global _lib
     if _lib is not None:
         return _lib
-    path = library_path()
-    if not os.path.exists(path):
-        build_oracle()
+    path = build_oracle()  # rebuilds when fp8_oracle.c is newer than the library
     lib = C.CDLL(path)
     sig = {
         "oracle_e4m3_decode": (C.c_double, [C.c_uint8]),
@@ -43,6 +41,10 @@ def load():
         "oracle_mx_scale_offset": (_I64, [_I64, _I64, _I64]),
         "oracle_mx_scale_bytes": (_I64, [_I64, _I64]),
         "oracle_quant_mx_1x32": (None, [_P, _I64, _I64, _I64, _P, _P]),
+        "oracle_pow2_exponent": (C.c_int, [C.c_float]),
+        "oracle_quant_group_1x128_pow2": (None, [_P, _I64, _I64, _I64, _P, _P]),
+        "oracle_quant_group_128x1_T_pow2": (None, [_P, _I64, _I64, _I64, _P, _P]),
+        "oracle_quant_block_128x128_pow2": (None, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
         "oracle_dequant_group": (None, [_P, _P, _I64, _I64, _P]),
         "oracle_dequant_block": (None, [_P, _P, _I64, _I64, _P]),
         "oracle_dequant_mx": (None, [_P, _P, _I64, _I64, _P]),
@@ -143,6 +145,44 @@ def quant_mx_1x32(x_bits):
     codes = np.empty((R, K), np.uint8)
     scales = np.empty((mx_scale_bytes(R, K),), np.uint8)
     load().oracle_quant_mx_1x32(_ptr(x), R, K, K, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def pow2_exponent(amax: float) -> int:
+    return int(load().oracle_pow2_exponent(float(amax)))
+
+
+def quant_group_1x128_pow2(x_bits):
+    """1x128 groups, power-of-two scales as E8M0 bytes in the MX atom layout."""
+    x = _bits(x_bits)
+    M, K = x.shape
+    codes = np.empty((M, K), np.uint8)
+    scales = np.empty((mx_scale_bytes(M, K),), np.uint8)
+    load().oracle_quant_group_1x128_pow2(_ptr(x), M, K, K, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def quant_group_128x1_T_pow2(x_bits):
+    x = _bits(x_bits)
+    M, K = x.shape
+    codes_t = np.empty((K, M), np.uint8)
+    scales_t = np.empty((mx_scale_bytes(K, M),), np.uint8)
+    load().oracle_quant_group_128x1_T_pow2(_ptr(x), M, K, K, _ptr(codes_t), _ptr(scales_t))
+    return codes_t, scales_t
+
+
+def quant_block_128x128_pow2(w_bits, transposed: bool = False):
+    w = _bits(w_bits)
+    N, K = w.shape
+    codes = np.empty((N, K), np.uint8)
+    scales = np.empty((mx_scale_bytes(N, K),), np.uint8)
+    if transposed:
+        codes_t = np.empty((K, N), np.uint8)
+        scales_t = np.empty((mx_scale_bytes(K, N),), np.uint8)
+        load().oracle_quant_block_128x128_pow2(_ptr(w), N, K, K, _ptr(codes), _ptr(scales),
+                                               _ptr(codes_t), _ptr(scales_t))
+        return codes, scales, codes_t, scales_t
+    load().oracle_quant_block_128x128_pow2(_ptr(w), N, K, K, _ptr(codes), _ptr(scales), None, None)
     return codes, scales
 
 

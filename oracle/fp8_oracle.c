@@ -353,6 +353,121 @@ void oracle_quant_mx_1x32(const uint16_t* x, int64_t R, int64_t K, int64_t ld,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Blockwise recipe with power-of-two scales ([P1] "Deep dive: FP8            */
+/* quantization with FP32 and power-of-two block scales": Blackwell's tensor  */
+/* cores take only power-of-two block scales, at the cost of a grid up to 2x  */
+/* coarser).  Same groups as the fp32 recipe (1x128, 128x1, 128x128); the     */
+/* scale is s = 2^e, e = ceil(log2(amax/448)) with amax/448 the fp32 scale of */
+/* the fp32 recipe, i.e. the smallest power of two not below it, so that      */
+/* max|x|/s <= 448; e clamped to the E8M0 range [-127, 127]; e = 0 (s = 1)    */
+/* for an all-zero group, as in the fp32 recipe.  Codes from the exact        */
+/* product x * 2^-e.  The scales are stored as E8M0 bytes (e + 127) in the    */
+/* MX scale-factor layout, each group's byte repeated in every 1x32 block it  */
+/* covers, so the tensor is also a valid MXFP8 tensor.                        */
+/* ------------------------------------------------------------------------ */
+
+int oracle_pow2_exponent(float amax)
+{
+    if (amax == 0.0f)
+        return 0;
+    float t = amax / 448.0f;                /* the fp32 recipe's scale */
+    int e = floor_log2_f32(t);
+    if ((double)t != ldexp(1.0, e))         /* not a power of two: round up */
+        e += 1;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+static uint8_t encode_pow2(float x, int e)
+{
+    return oracle_e4m3_encode_f64(ldexp((double)x, -e));
+}
+
+/* x: bf16 [M][ld], K % 128 == 0.  codes [M][K]; scales: MX atoms of [M][K]. */
+void oracle_quant_group_1x128_pow2(const uint16_t* x, int64_t M, int64_t K, int64_t ld,
+                                   uint8_t* codes, uint8_t* scales)
+{
+    memset(scales, 0, (size_t)oracle_mx_scale_bytes(M, K));
+    int64_t G = K / 128;
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < M; ++r) {
+        for (int64_t g = 0; g < G; ++g) {
+            float amax = 0.0f;
+            for (int64_t j = 0; j < 128; ++j) {
+                float a = fabsf(bf16_bits_to_f32(x[r * ld + g * 128 + j]));
+                if (a > amax) amax = a;
+            }
+            int e = oracle_pow2_exponent(amax);
+            for (int64_t b = 0; b < 4; ++b)
+                scales[oracle_mx_scale_offset(r, 4 * g + b, K)] = (uint8_t)(e + 127);
+            for (int64_t j = 0; j < 128; ++j)
+                codes[r * K + g * 128 + j] = encode_pow2(bf16_bits_to_f32(x[r * ld + g * 128 + j]), e);
+        }
+    }
+}
+
+/* 128x1 groups, codes transposed: codesT [K][M] (the WGrad operand, M
+ * contiguous); scales: MX atoms of the transposed [K][M] tensor, i.e. the
+ * 1x32 blocks run along M.  M % 128 == 0. */
+void oracle_quant_group_128x1_T_pow2(const uint16_t* x, int64_t M, int64_t K, int64_t ld,
+                                     uint8_t* codesT, uint8_t* scalesT)
+{
+    memset(scalesT, 0, (size_t)oracle_mx_scale_bytes(K, M));
+    int64_t B = M / 128;
+    #pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < K; ++c) {
+        for (int64_t b = 0; b < B; ++b) {
+            float amax = 0.0f;
+            for (int64_t i = 0; i < 128; ++i) {
+                float a = fabsf(bf16_bits_to_f32(x[(b * 128 + i) * ld + c]));
+                if (a > amax) amax = a;
+            }
+            int e = oracle_pow2_exponent(amax);
+            for (int64_t q = 0; q < 4; ++q)
+                scalesT[oracle_mx_scale_offset(c, 4 * b + q, M)] = (uint8_t)(e + 127);
+            for (int64_t i = 0; i < 128; ++i)
+                codesT[c * M + b * 128 + i] = encode_pow2(bf16_bits_to_f32(x[(b * 128 + i) * ld + c]), e);
+        }
+    }
+}
+
+/* 128x128 blocks: codes [N][K], scales MX atoms of [N][K]; optionally the
+ * transposed copy codesT [K][N] with MX atoms of [K][N] (same exponents). */
+void oracle_quant_block_128x128_pow2(const uint16_t* w, int64_t N, int64_t K, int64_t ld,
+                                     uint8_t* codes, uint8_t* scales,
+                                     uint8_t* codesT, uint8_t* scalesT)
+{
+    memset(scales, 0, (size_t)oracle_mx_scale_bytes(N, K));
+    if (scalesT) memset(scalesT, 0, (size_t)oracle_mx_scale_bytes(K, N));
+    int64_t NB = N / 128, KB = K / 128;
+    #pragma omp parallel for schedule(static)
+    for (int64_t nb = 0; nb < NB; ++nb) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            float amax = 0.0f;
+            for (int64_t i = 0; i < 128; ++i)
+                for (int64_t j = 0; j < 128; ++j) {
+                    float a = fabsf(bf16_bits_to_f32(w[(nb * 128 + i) * ld + kb * 128 + j]));
+                    if (a > amax) amax = a;
+                }
+            int e = oracle_pow2_exponent(amax);
+            for (int64_t i = 0; i < 128; ++i)
+                for (int64_t q = 0; q < 4; ++q) {
+                    scales[oracle_mx_scale_offset(nb * 128 + i, 4 * kb + q, K)] = (uint8_t)(e + 127);
+                    if (scalesT) scalesT[oracle_mx_scale_offset(kb * 128 + i, 4 * nb + q, N)] = (uint8_t)(e + 127);
+                }
+            for (int64_t i = 0; i < 128; ++i)
+                for (int64_t j = 0; j < 128; ++j) {
+                    int64_t n = nb * 128 + i, k = kb * 128 + j;
+                    uint8_t q = encode_pow2(bf16_bits_to_f32(w[n * ld + k]), e);
+                    codes[n * K + k] = q;
+                    if (codesT) codesT[k * N + n] = q;
+                }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Dequantization (exact in fp64: a 4-bit significand times a 24-bit scale).  */
 /* ------------------------------------------------------------------------ */
 
