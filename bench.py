@@ -225,7 +225,21 @@ def breakdown(fp8, synth, dev, flush, pk, reps):
     rec("sync_install", time_kernel(lambda: fp8.sync_install(payload, [fp8.SyncEntry(1, rollout)], check=False),
                                     flush, reps),
         bytes_=2 * pb, workload=f"W 12288x4096 payload {pb} B")
-    del X, W, qx, qw, Y, Y2, qy, payload, rollout
+    # the same forward with power-of-two block scales: the GEMM runs on the
+    # block-scaled MMA (no promotion)
+    px = fp8.quantize_group(X, "K", pow2=True)
+    pw = fp8.quantize_block(W, pow2=True)
+    rec("quant_group_1x128_pow2", time_kernel(lambda: fp8.quantize_group(X, "K", out=px, pow2=True), flush, reps),
+        bytes_=M * K * (3 + 4 / 128), workload="X 8192x4096, power-of-two scales")
+    rec("quant_block_128x128_pow2", time_kernel(lambda: fp8.quantize_block(W, out=pw, pow2=True), flush, reps),
+        bytes_=N * K * (3 + 1 / 32), workload="W 12288x4096, power-of-two scales")
+    rec("gemm_blockwise_pow2_fwd", time_kernel(lambda: fp8.gemm(px, pw, out=Y), flush, reps),
+        flops=2.0 * M * N * K, workload="8192x4096x12288, power-of-two scales")
+    Y3, qy3 = fp8.gemm(px, pw, quantize_output=True)
+    rec("gemm_blockwise_pow2_fwd_fused_quant",
+        time_kernel(lambda: fp8.gemm(px, pw, quantize_output=True, out=Y3, out_q=qy3), flush, reps),
+        flops=2.0 * M * N * K, workload="8192x4096x12288 + 1x128 power-of-two quant of Y")
+    del X, W, qx, qw, Y, Y2, qy, payload, rollout, px, pw, Y3, qy3
     torch.cuda.empty_cache()
 
     # backward
@@ -284,12 +298,13 @@ def breakdown(fp8, synth, dev, flush, pk, reps):
 
 def _case_gemm(kind):
     def setup(fp8, synth, dev):
-        if kind in ("fwd", "fwd_fused"):
+        if kind in ("fwd", "fwd_fused", "pow2", "pow2_fused"):
             wl = synth.mlp()
             X, W = wl.tensors["X"].to(dev), wl.tensors["W"].to(dev)
-            qx, qw = fp8.quantize_group(X, "K"), fp8.quantize_block(W)
+            p2 = kind.startswith("pow2")
+            qx, qw = fp8.quantize_group(X, "K", pow2=p2), fp8.quantize_block(W, pow2=p2)
             Y, qy = fp8.gemm(qx, qw, quantize_output=True)
-            if kind == "fwd":
+            if kind in ("fwd", "pow2"):
                 return lambda: fp8.gemm(qx, qw, out=Y), 2.0 * M * N * K
             return lambda: fp8.gemm(qx, qw, quantize_output=True, out=Y, out_q=qy), 2.0 * M * N * K
         if kind in ("dgrad", "wgrad"):
@@ -341,6 +356,7 @@ KERNEL_CASES = {
     "gemm_blockwise_fwd": _case_gemm("fwd"), "gemm_blockwise_fwd_fused": _case_gemm("fwd_fused"),
     "gemm_blockwise_dgrad": _case_gemm("dgrad"), "gemm_blockwise_wgrad": _case_gemm("wgrad"),
     "gemm_mx_fwd": _case_gemm("mx"), "gemm_mx_grouped": _case_gemm("grouped"),
+    "gemm_blockwise_pow2_fwd": _case_gemm("pow2"), "gemm_blockwise_pow2_fwd_fused": _case_gemm("pow2_fused"),
     "quant_group_1x128": _case_quant("group_k"), "quant_block_128x128": _case_quant("block"),
     "quant_group_128x1_T": _case_quant("group_m"), "quant_mx_1x32": _case_quant("mx"),
 }

@@ -21,14 +21,14 @@ __all__ = [
     "FP8Error", "QTensor", "SyncEntry", "library", "quantize_group", "quantize_block", "quantize_mx",
     "permute_rows_mx", "gemm", "grouped_gemm", "sync_payload_size", "sync_pack", "sync_install", "sync_install_noalloc",
     "status_poll", "mx_scale_bytes", "mx_grouped_scale_bytes",
-    "RECIPE_BLOCKWISE", "RECIPE_MX", "LAYOUT_GROUP_1x128", "LAYOUT_BLOCK_128x128", "LAYOUT_MX_1x32",
+    "RECIPE_BLOCKWISE", "RECIPE_MX", "RECIPE_BLOCKWISE_POW2", "LAYOUT_GROUP_1x128", "LAYOUT_BLOCK_128x128", "LAYOUT_MX_1x32",
     "LAYOUT_MX_1x32_GROUPED",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8bs.so")
 
-RECIPE_BLOCKWISE, RECIPE_MX = 1, 2
+RECIPE_BLOCKWISE, RECIPE_MX, RECIPE_BLOCKWISE_POW2 = 1, 2, 3
 LAYOUT_GROUP_1x128, LAYOUT_BLOCK_128x128, LAYOUT_MX_1x32, LAYOUT_MX_1x32_GROUPED = 1, 2, 3, 4
 AXIS_K, AXIS_M = 0, 1
 OP = {"fwd": 0, "dgrad": 1, "wgrad": 2}
@@ -144,22 +144,30 @@ def _bf16_2d(x: torch.Tensor) -> torch.Tensor:
 
 
 # ---------------------------------------------------------------- quantizers
-def quantize_group(x: torch.Tensor, axis: str = "K", out: Optional[QTensor] = None, stream=None) -> QTensor:
+def _scales_for(rows: int, cols: int, pow2: bool, fp32_shape, dev) -> torch.Tensor:
+    if pow2:
+        return torch.empty((mx_scale_bytes(rows, cols),), dtype=torch.uint8, device=dev)
+    return torch.empty(fp32_shape, dtype=torch.float32, device=dev)
+
+
+def quantize_group(x: torch.Tensor, axis: str = "K", out: Optional[QTensor] = None, stream=None,
+                   pow2: bool = False) -> QTensor:
     """1x128 groups along K (axis='K') or 128x1 groups along M written
-    transposed (axis='M', the WGrad operand layout).  `out` may supply
-    preallocated codes/scales."""
+    transposed (axis='M', the WGrad operand layout).  pow2=True: power-of-two
+    scales as E8M0 bytes in the MX layout (RECIPE_BLOCKWISE_POW2).  `out`
+    may supply preallocated codes/scales."""
     x = _bf16_2d(x)
     M, K = x.shape
     dev = _dev(x)
+    recipe = RECIPE_BLOCKWISE_POW2 if pow2 else RECIPE_BLOCKWISE
+    layout = LAYOUT_MX_1x32 if pow2 else LAYOUT_GROUP_1x128
     if axis == "K":
         q = out or QTensor(torch.empty((M, K), dtype=torch.uint8, device=dev),
-                    torch.empty((K // 128, M), dtype=torch.float32, device=dev), M, K, RECIPE_BLOCKWISE,
-                    LAYOUT_GROUP_1x128)
+                           _scales_for(M, K, pow2, (K // 128, M), dev), M, K, recipe, layout)
         ax = AXIS_K
     elif axis == "M":
         q = out or QTensor(torch.empty((K, M), dtype=torch.uint8, device=dev),
-                    torch.empty((M // 128, K), dtype=torch.float32, device=dev), K, M, RECIPE_BLOCKWISE,
-                    LAYOUT_GROUP_1x128)
+                           _scales_for(K, M, pow2, (M // 128, K), dev), K, M, recipe, layout)
         ax = AXIS_M
     else:
         raise FP8Error(1, f"axis must be 'K' or 'M', got {axis!r}")
@@ -169,20 +177,21 @@ def quantize_group(x: torch.Tensor, axis: str = "K", out: Optional[QTensor] = No
 
 
 def quantize_block(w: torch.Tensor, transposed: bool = False, out: Optional[QTensor] = None,
-                   out_t: Optional[QTensor] = None, stream=None):
+                   out_t: Optional[QTensor] = None, stream=None, pow2: bool = False):
     """128x128 blocks; with transposed=True also returns the transposed copy
-    (codes [K, N], scales [K/128, N/128]) used as the DGrad B operand."""
+    (codes [K, N], scales [K/128, N/128]) used as the DGrad B operand.
+    pow2=True: power-of-two scales in the MX layout (RECIPE_BLOCKWISE_POW2)."""
     w = _bf16_2d(w)
     N, K = w.shape
     dev = _dev(w)
+    recipe = RECIPE_BLOCKWISE_POW2 if pow2 else RECIPE_BLOCKWISE
+    layout = LAYOUT_MX_1x32 if pow2 else LAYOUT_BLOCK_128x128
     q = out or QTensor(torch.empty((N, K), dtype=torch.uint8, device=dev),
-                torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev), N, K, RECIPE_BLOCKWISE,
-                LAYOUT_BLOCK_128x128)
+                       _scales_for(N, K, pow2, (N // 128, K // 128), dev), N, K, recipe, layout)
     qt = None
     if transposed:
         qt = out_t or QTensor(torch.empty((K, N), dtype=torch.uint8, device=dev),
-                     torch.empty((K // 128, N // 128), dtype=torch.float32, device=dev), K, N,
-                     RECIPE_BLOCKWISE, LAYOUT_BLOCK_128x128)
+                              _scales_for(K, N, pow2, (K // 128, N // 128), dev), K, N, recipe, layout)
     t = q.c()
     tt = qt.c() if qt is not None else None
     _check(library().fp8_quantize_block(w.data_ptr(), N, K, w.stride(0), C.byref(t),
@@ -225,7 +234,8 @@ def permute_rows_mx(q: QTensor, gather: torch.Tensor, offsets: torch.Tensor, out
 def gemm(A: QTensor, B: QTensor, op: str = "fwd", out_dtype=torch.bfloat16, quantize_output: bool = False,
          out: Optional[torch.Tensor] = None, out_q: Optional[QTensor] = None, stream=None):
     """D = A B^T with fp32 accumulation.  Returns D, or (D, QTensor of D)
-    when quantize_output (1x128 for blockwise, 1x32 for MXFP8)."""
+    when quantize_output (1x128 for blockwise, 1x32 for MXFP8, 1x128 with
+    power-of-two scales for the blockwise power-of-two recipe)."""
     M, N = A.rows, B.rows
     dev = _dev(A.codes)
     if out is None:
@@ -238,7 +248,7 @@ def gemm(A: QTensor, B: QTensor, op: str = "fwd", out_dtype=torch.bfloat16, quan
                          LAYOUT_GROUP_1x128)
         else:
             dq = QTensor(torch.empty((M, N), dtype=torch.uint8, device=dev),
-                         torch.empty((mx_scale_bytes(M, N),), dtype=torch.uint8, device=dev), M, N, RECIPE_MX,
+                         torch.empty((mx_scale_bytes(M, N),), dtype=torch.uint8, device=dev), M, N, A.recipe,
                          LAYOUT_MX_1x32)
     a, b = A.c(), B.c()
     dqc = dq.c() if dq is not None else None

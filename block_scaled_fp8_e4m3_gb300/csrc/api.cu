@@ -136,7 +136,8 @@ fp8_status entry_bytes(const fp8_sync_entry& e, int i, uint64_t* db, uint64_t* s
     else if (t.recipe == FP8_RECIPE_BLOCKWISE_FP32 && t.layout == FP8_LAYOUT_BLOCK_128x128 && t.rows % 128 == 0 &&
              t.cols % 128 == 0)
         *sb = (uint64_t)((t.rows / 128) * (t.cols / 128) * 4);
-    else if (t.recipe == FP8_RECIPE_MXFP8 && t.layout == FP8_LAYOUT_MX_1x32 && t.cols % 32 == 0)
+    else if ((t.recipe == FP8_RECIPE_MXFP8 || t.recipe == FP8_RECIPE_BLOCKWISE_POW2) &&
+             t.layout == FP8_LAYOUT_MX_1x32 && t.cols % 32 == 0)
         *sb = (uint64_t)mx_scale_bytes(t.rows, t.cols);
     else
         return fail(FP8_ERR_UNSUPPORTED, "entry %d: recipe %d / layout %d / shape %lldx%lld cannot be synced", i,
@@ -339,10 +340,12 @@ fp8_status fp8_quantize_group(const void* x_bf16, int64_t M, int64_t K, int64_t 
     if (s != FP8_OK) return s;
     if (axis == FP8_AXIS_K) {
         if (K % 128 != 0) return fail(FP8_ERR_UNSUPPORTED, "1x128 groups need K %% 128 == 0 (K = %lld)", (long long)K);
-        s = check_out(out, "out", FP8_RECIPE_BLOCKWISE_FP32, FP8_LAYOUT_GROUP_1x128, M, K);
+        const bool pow2 = out != nullptr && out->recipe == FP8_RECIPE_BLOCKWISE_POW2;
+        s = pow2 ? check_out(out, "out", FP8_RECIPE_BLOCKWISE_POW2, FP8_LAYOUT_MX_1x32, M, K)
+                 : check_out(out, "out", FP8_RECIPE_BLOCKWISE_FP32, FP8_LAYOUT_GROUP_1x128, M, K);
         if (s != FP8_OK) return s;
         cudaError_t e = launch_quant_group_k(static_cast<const uint16_t*>(x_bf16), M, K, ld,
-                                             static_cast<uint8_t*>(out->codes), static_cast<float*>(out->scales),
+                                             static_cast<uint8_t*>(out->codes), out->scales, pow2,
                                              reinterpret_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? FP8_OK : cuda_fail(e, "quantize_group(K)");
     }
@@ -350,10 +353,12 @@ fp8_status fp8_quantize_group(const void* x_bf16, int64_t M, int64_t K, int64_t 
         if (M % 128 != 0 || K % 8 != 0)
             return fail(FP8_ERR_UNSUPPORTED, "128x1 groups need M %% 128 == 0 and K %% 8 == 0 (M = %lld, K = %lld)",
                         (long long)M, (long long)K);
-        s = check_out(out, "out", FP8_RECIPE_BLOCKWISE_FP32, FP8_LAYOUT_GROUP_1x128, K, M);
+        const bool pow2 = out != nullptr && out->recipe == FP8_RECIPE_BLOCKWISE_POW2;
+        s = pow2 ? check_out(out, "out", FP8_RECIPE_BLOCKWISE_POW2, FP8_LAYOUT_MX_1x32, K, M)
+                 : check_out(out, "out", FP8_RECIPE_BLOCKWISE_FP32, FP8_LAYOUT_GROUP_1x128, K, M);
         if (s != FP8_OK) return s;
         cudaError_t e = launch_quant_group_m(static_cast<const uint16_t*>(x_bf16), M, K, ld,
-                                             static_cast<uint8_t*>(out->codes), static_cast<float*>(out->scales),
+                                             static_cast<uint8_t*>(out->codes), out->scales, pow2,
                                              reinterpret_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? FP8_OK : cuda_fail(e, "quantize_group(M)");
     }
@@ -367,17 +372,18 @@ fp8_status fp8_quantize_block(const void* w_bf16, int64_t N, int64_t K, int64_t 
     if (N % 128 != 0 || K % 128 != 0)
         return fail(FP8_ERR_UNSUPPORTED, "128x128 blocks need N, K multiples of 128 (N = %lld, K = %lld)", (long long)N,
                     (long long)K);
-    s = check_out(out, "out", FP8_RECIPE_BLOCKWISE_FP32, FP8_LAYOUT_BLOCK_128x128, N, K);
+    const bool pow2 = out != nullptr && out->recipe == FP8_RECIPE_BLOCKWISE_POW2;
+    const int recipe = pow2 ? FP8_RECIPE_BLOCKWISE_POW2 : FP8_RECIPE_BLOCKWISE_FP32;
+    const int layout = pow2 ? FP8_LAYOUT_MX_1x32 : FP8_LAYOUT_BLOCK_128x128;
+    s = check_out(out, "out", recipe, layout, N, K);
     if (s != FP8_OK) return s;
     if (out_t != nullptr) {
-        s = check_out(out_t, "out_t", FP8_RECIPE_BLOCKWISE_FP32, FP8_LAYOUT_BLOCK_128x128, K, N);
+        s = check_out(out_t, "out_t", recipe, layout, K, N);
         if (s != FP8_OK) return s;
     }
     cudaError_t e = launch_quant_block(static_cast<const uint16_t*>(w_bf16), N, K, ld, static_cast<uint8_t*>(out->codes),
-                                       static_cast<float*>(out->scales),
-                                       out_t ? static_cast<uint8_t*>(out_t->codes) : nullptr,
-                                       out_t ? static_cast<float*>(out_t->scales) : nullptr,
-                                       reinterpret_cast<cudaStream_t>(stream));
+                                       out->scales, out_t ? static_cast<uint8_t*>(out_t->codes) : nullptr,
+                                       out_t ? out_t->scales : nullptr, pow2, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FP8_OK : cuda_fail(e, "quantize_block");
 }
 
@@ -477,18 +483,24 @@ fp8_status fp8_gemm_blockscaled(const fp8_tensor* A, const fp8_tensor* B, void* 
         cudaError_t e = launch_gemm_blockwise(a, st, cs);
         return e == cudaSuccess ? FP8_OK : cuda_fail(e, "gemm_blockscaled(blockwise)");
     }
-    if (A->recipe == FP8_RECIPE_MXFP8) {
-        if (op != FP8_GEMM_FWD) return fail(FP8_ERR_UNSUPPORTED, "MXFP8 GEMM supports FP8_GEMM_FWD only");
-        if (d_dtype != FP8_OUT_BF16) return fail(FP8_ERR_UNSUPPORTED, "MXFP8 GEMM writes bf16 only");
-        s = check_out(A, "A", FP8_RECIPE_MXFP8, FP8_LAYOUT_MX_1x32, M, K);
+    if (A->recipe == FP8_RECIPE_MXFP8 || A->recipe == FP8_RECIPE_BLOCKWISE_POW2) {
+        // both run on the block-scaled MMA; the power-of-two blockwise
+        // recipe's scales are MX scales constant over each group
+        const int recipe = A->recipe;
+        const bool pow2 = recipe == FP8_RECIPE_BLOCKWISE_POW2;
+        if (!pow2 && op != FP8_GEMM_FWD) return fail(FP8_ERR_UNSUPPORTED, "MXFP8 GEMM supports FP8_GEMM_FWD only");
+        if (op != FP8_GEMM_FWD && op != FP8_GEMM_DGRAD && op != FP8_GEMM_WGRAD)
+            return fail(FP8_ERR_INVALID_ARG, "unknown op %d", op);
+        if (d_dtype != FP8_OUT_BF16) return fail(FP8_ERR_UNSUPPORTED, "this recipe's GEMM writes bf16 only");
+        s = check_out(A, "A", recipe, FP8_LAYOUT_MX_1x32, M, K);
         if (s != FP8_OK) return s;
-        s = check_out(B, "B", FP8_RECIPE_MXFP8, FP8_LAYOUT_MX_1x32, N, K);
+        s = check_out(B, "B", recipe, FP8_LAYOUT_MX_1x32, N, K);
         if (s != FP8_OK) return s;
         uint8_t* qc = nullptr;
         uint8_t* qs = nullptr;
         if (d_quant != nullptr) {
-            if (N % 128 != 0) return fail(FP8_ERR_UNSUPPORTED, "fused MX quantization needs N %% 128 == 0");
-            s = check_out(d_quant, "d_quant", FP8_RECIPE_MXFP8, FP8_LAYOUT_MX_1x32, M, N);
+            if (N % 128 != 0) return fail(FP8_ERR_UNSUPPORTED, "fused quantization needs N %% 128 == 0");
+            s = check_out(d_quant, "d_quant", recipe, FP8_LAYOUT_MX_1x32, M, N);
             if (s != FP8_OK) return s;
             qc = static_cast<uint8_t*>(d_quant->codes);
             qs = static_cast<uint8_t*>(d_quant->scales);
@@ -507,6 +519,7 @@ fp8_status fp8_gemm_blockscaled(const fp8_tensor* A, const fp8_tensor* B, void* 
         a.ldd = ldd;
         a.q_codes = qc;
         a.q_scales = qs;
+        a.q_pow2 = pow2;
         cudaError_t e = launch_gemm_mx(a, st, cs);
         return e == cudaSuccess ? FP8_OK : cuda_fail(e, "gemm_blockscaled(mx)");
     }

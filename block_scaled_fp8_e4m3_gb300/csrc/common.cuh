@@ -136,6 +136,25 @@ __device__ __forceinline__ float exp2_int(int k) {
     return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(0x00400000u);
 }
 
+// Exponent of the blockwise recipe's power-of-two scale: e = ceil(log2(t)),
+// t = RN(amax/448) the fp32 recipe's scale, i.e. the smallest power of two
+// not below t; clamped to the E8M0 range [-127, 127]; 0 (s = 1) for an
+// all-zero group.  amax is a bf16 value or +inf.
+__device__ __forceinline__ int pow2_exponent(float amax) {
+    if (amax == 0.0f) return 0;
+    const uint32_t u = __float_as_uint(group_scale_bf16(amax));
+    const int bexp = (int)(u >> 23);
+    const uint32_t m = u & 0x7FFFFFu;
+    int e;
+    if (bexp == 0xFF)
+        e = 127;
+    else if (bexp != 0)
+        e = bexp - 127 + (m != 0u ? 1 : 0);
+    else
+        e = (31 - __clz(m)) - 149 + ((m & (m - 1u)) != 0u ? 1 : 0);
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
 // Byte offset of the E8M0 scale of (row r, 32-column block j) in the
 // 128x4 atom layout (atoms_k = ceil(cols/128) atoms per 128-row tile).
 __device__ __forceinline__ int64_t mx_scale_offset(int64_t r, int64_t j, int64_t atoms_k) {

@@ -55,6 +55,29 @@ __device__ __forceinline__ uint32_t quant_row_mx(const uint32_t (&packed)[64], u
     return sc;
 }
 
+// The same 128 values as one 1x128 group with a power-of-two scale (the
+// blockwise recipe's Blackwell variant): one exponent, repeated in the four
+// returned E8M0 bytes.
+__device__ __forceinline__ uint32_t quant_row_pow2(const uint32_t (&packed)[64], uint8_t* codes) {
+    float a = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 64; ++j) a = fmaxf(a, fmaxf(fabsf(bf16_lo(packed[j])), fabsf(bf16_hi(packed[j]))));
+    const int e = pow2_exponent(a);
+    const float mul = exp2_int(-e);
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t p0 = packed[8 * b + 2 * k], p1 = packed[8 * b + 2 * k + 1];
+            w[k] = e4m3x2(__fmul_rn(bf16_lo(p0), mul), __fmul_rn(bf16_hi(p0), mul)) |
+                   (e4m3x2(__fmul_rn(bf16_lo(p1), mul), __fmul_rn(bf16_hi(p1), mul)) << 16);
+        }
+        reinterpret_cast<uint4*>(codes)[b] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    return (uint32_t)(e + 127) * 0x01010101u;
+}
+
 // ===========================================================================
 // MXFP8 GEMM (hardware block scaling), plain or grouped
 // ===========================================================================
@@ -70,7 +93,8 @@ struct MxParams {
     uint8_t* q_scales;
     StatusBlock* st;
     int tiles_n;
-    int d_v8;  // D rows allow 32-byte stores
+    int d_v8;    // D rows allow 32-byte stores
+    int q_pow2;  // fused quantization: 1x128 groups, power-of-two scales
 };
 
 struct TileCoord {
@@ -310,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
                 }
                 if (p.q_codes != nullptr) {
-                    const uint32_t sc = quant_row_mx(packed, p.q_codes + m * p.N + ncol0);
+                    const uint32_t sc = p.q_pow2 ? quant_row_pow2(packed, p.q_codes + m * p.N + ncol0)
+                                                 : quant_row_mx(packed, p.q_codes + m * p.N + ncol0);
                     *reinterpret_cast<uint32_t*>(p.q_scales + mx_scale_offset(m, ncol0 / 32, q_atoms_k)) = sc;
                 }
             } else if (p.q_codes != nullptr && hvalid && m < ((int64_t)p.M + 127) / 128 * 128) {
@@ -358,6 +383,7 @@ cudaError_t launch_gemm_mx(const GemmMxArgs& a, StatusBlock* status, cudaStream_
     p.ldd = a.ldd;
     p.q_codes = a.q_codes;
     p.q_scales = a.q_scales;
+    p.q_pow2 = a.q_pow2 ? 1 : 0;
     p.st = status;
     p.tiles_n = (int)((a.N + kMxBN - 1) / kMxBN);
     p.d_v8 = (reinterpret_cast<uintptr_t>(a.D) % 32 == 0) && ((a.ldd * 2) % 32 == 0);

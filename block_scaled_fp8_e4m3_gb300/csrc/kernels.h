@@ -11,12 +11,14 @@ namespace fp8bs {
 struct StatusBlock;
 
 // quantize.cu
+// pow2: the blockwise recipe with power-of-two scales, written as E8M0 bytes
+// in the MX scale-factor layout (scales then points to bytes, not floats)
 cudaError_t launch_quant_group_k(const uint16_t* x, int64_t M, int64_t K, int64_t ld, uint8_t* codes,
-                                 float* scales, cudaStream_t st);
+                                 void* scales, bool pow2, cudaStream_t st);
 cudaError_t launch_quant_group_m(const uint16_t* x, int64_t M, int64_t K, int64_t ld, uint8_t* codes_t,
-                                 float* scales, cudaStream_t st);
+                                 void* scales, bool pow2, cudaStream_t st);
 cudaError_t launch_quant_block(const uint16_t* w, int64_t N, int64_t K, int64_t ld, uint8_t* codes,
-                               float* scales, uint8_t* codes_t, float* scales_t, cudaStream_t st);
+                               void* scales, uint8_t* codes_t, void* scales_t, bool pow2, cudaStream_t st);
 cudaError_t launch_quant_mx(const uint16_t* x, int64_t R, int64_t K, int64_t ld, uint8_t* codes, uint8_t* scales,
                             cudaStream_t st);
 cudaError_t launch_permute_rows_mx(const uint8_t* src_codes, const uint8_t* src_scales, int64_t src_rows,
@@ -53,6 +55,7 @@ struct GemmMxArgs {
     int64_t ldd;
     uint8_t* q_codes;          // fused MX quantization of D (nullable; single group only)
     uint8_t* q_scales;
+    bool q_pow2 = false;       // fused quantization in 1x128 groups with power-of-two scales
 };
 cudaError_t launch_gemm_mx(const GemmMxArgs& a, StatusBlock* status, cudaStream_t st);
 

@@ -85,9 +85,12 @@ __device__ __forceinline__ void encode16(const uint4 (&v)[2], const Divider& d, 
     }
 }
 
+// kPow2: power-of-two scales, E8M0 bytes in the MX layout, each group's
+// byte in its four 1x32 slots (one 32-bit store per row and group).
+template <bool kPow2>
 __global__ void __launch_bounds__(256, 4) k_quant_group_k(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                           int64_t ld, uint8_t* __restrict__ codes,
-                                                          float* __restrict__ scales) {
+                                                          void* __restrict__ scales) {
     const int G = (int)(K / 128);
     const int gchunks = (G + kGK_Groups - 1) / kGK_Groups;
     const int strip = (int)(blockIdx.x / (unsigned)gchunks);
@@ -120,13 +123,30 @@ __global__ void __launch_bounds__(256, 4) k_quant_group_k(const uint16_t* __rest
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        const float sc = group_scale_bf16(a);
         uint2 c[2];
-        encode16(v[u], make_divider(sc), c);
-        if (row_ok && g < G) {
-            *reinterpret_cast<uint2*>(cr + g * 128) = c[0];
-            *reinterpret_cast<uint2*>(cr + g * 128 + 64) = c[1];
-            if (sub == 0) scales[(int64_t)g * M + row] = sc;
+        if (kPow2) {
+            const int e = pow2_exponent(a);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float f[8];
+                unpack8(v[u][h], f);
+                c[h] = encode8_mul(f, exp2_int(-e));
+            }
+            if (row_ok && g < G) {
+                *reinterpret_cast<uint2*>(cr + g * 128) = c[0];
+                *reinterpret_cast<uint2*>(cr + g * 128 + 64) = c[1];
+                if (sub == 0)
+                    *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scales) + mx_scale_offset(row, 4 * g, G)) =
+                        (uint32_t)(e + 127) * 0x01010101u;
+            }
+        } else {
+            const float sc = group_scale_bf16(a);
+            encode16(v[u], make_divider(sc), c);
+            if (row_ok && g < G) {
+                *reinterpret_cast<uint2*>(cr + g * 128) = c[0];
+                *reinterpret_cast<uint2*>(cr + g * 128 + 64) = c[1];
+                if (sub == 0) static_cast<float*>(scales)[(int64_t)g * M + row] = sc;
+            }
         }
     }
 }
@@ -139,9 +159,10 @@ __global__ void __launch_bounds__(256, 4) k_quant_group_k(const uint16_t* __rest
 // a column's 4 rows form one 32-bit word of the transposed tile in shared
 // memory (column stride 33 words), which is written out 16 bytes per thread.
 // ---------------------------------------------------------------------------
+template <bool kPow2>
 __global__ void __launch_bounds__(256) k_quant_group_m(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                        int64_t ld, uint8_t* __restrict__ codes_t,
-                                                       float* __restrict__ scales) {
+                                                       void* __restrict__ scales) {
     __shared__ float red[8][64];
     __shared__ float col_scale[64], col_rcp[64];
     __shared__ uint32_t tile[64 * 33];
@@ -179,19 +200,35 @@ __global__ void __launch_bounds__(256) k_quant_group_m(const uint16_t* __restric
         float a = red[0][t];
 #pragma unroll
         for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w][t]);
-        const float s = group_scale_bf16(a);
-        col_scale[t] = s;
-        col_rcp[t] = __frcp_rn(s);
-        if (c0 + t < K) scales[mb * K + c0 + t] = s;
+        if (kPow2) {
+            // transposed row c0+t of the [K][M] output, 1x32 blocks 4mb..4mb+3
+            const int e = pow2_exponent(a);
+            col_scale[t] = exp2_int(-e);
+            if (c0 + t < K)
+                *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scales) + mx_scale_offset(c0 + t, 4 * mb, M / 128)) =
+                    (uint32_t)(e + 127) * 0x01010101u;
+        } else {
+            const float s = group_scale_bf16(a);
+            col_scale[t] = s;
+            col_rcp[t] = __frcp_rn(s);
+            if (c0 + t < K) static_cast<float*>(scales)[mb * K + c0 + t] = s;
+        }
     }
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
+        float q[4];
+        if (kPow2) {
+            const float mul = col_scale[chunk * 8 + j];  // exact power of two
+#pragma unroll
+            for (int i = 0; i < 4; ++i) q[i] = __fmul_rn(f[i][j], mul);
+            tile[(chunk * 8 + j) * 33 + quad] = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
+            continue;
+        }
         Divider dv;
         dv.s = col_scale[chunk * 8 + j];
         dv.r = col_rcp[chunk * 8 + j];
         dv.fast = dv.s >= 0x1p-100f && dv.s <= 3.402823466e38f;
-        float q[4];
         if (dv.fast) {
             quotient2_fast(dv, f[0][j], f[1][j], q[0], q[1]);
             quotient2_fast(dv, f[2][j], f[3][j], q[2], q[3]);
@@ -225,10 +262,11 @@ __global__ void __launch_bounds__(256) k_quant_group_m(const uint16_t* __restric
 // goes through a shared-memory tile (row stride 144 B) read column-wise; each
 // thread writes 32 contiguous transposed bytes (one full sector).
 // ---------------------------------------------------------------------------
+template <bool kPow2>
 __global__ void __launch_bounds__(256) k_quant_block(const uint16_t* __restrict__ w, int64_t N, int64_t K,
                                                      int64_t ld, uint8_t* __restrict__ codes,
-                                                     float* __restrict__ scales, uint8_t* __restrict__ codes_t,
-                                                     float* __restrict__ scales_t) {
+                                                     void* __restrict__ scales, uint8_t* __restrict__ codes_t,
+                                                     void* __restrict__ scales_t) {
     constexpr int kStride = 144;
     __shared__ float red[8];
     __shared__ __align__(16) uint8_t tile[128 * kStride];
@@ -256,17 +294,31 @@ __global__ void __launch_bounds__(256) k_quant_block(const uint16_t* __restrict_
     a = red[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) a = fmaxf(a, red[i]);
-    const float s = group_scale_bf16(a);
-    if (t == 0) {
-        scales[nb * KB + kb] = s;
-        if (scales_t) scales_t[kb * NB + nb] = s;
+    Divider dv;
+    float mul = 1.0f;
+    if (kPow2) {
+        // the block's exponent fills its whole 512-byte MX atom (and the
+        // transposed copy's atom): 16 bytes per thread of the first warps
+        const int e = pow2_exponent(a);
+        mul = exp2_int(-e);
+        const uint32_t b4 = (uint32_t)(e + 127) * 0x01010101u;
+        const uint4 fill = make_uint4(b4, b4, b4, b4);
+        if (t < 32) reinterpret_cast<uint4*>(static_cast<uint8_t*>(scales) + (nb * KB + kb) * 512)[t] = fill;
+        else if (t < 64 && scales_t)
+            reinterpret_cast<uint4*>(static_cast<uint8_t*>(scales_t) + (kb * NB + nb) * 512)[t - 32] = fill;
+    } else {
+        const float s = group_scale_bf16(a);
+        if (t == 0) {
+            static_cast<float*>(scales)[nb * KB + kb] = s;
+            if (scales_t) static_cast<float*>(scales_t)[kb * NB + nb] = s;
+        }
+        dv = make_divider(s);
     }
-    const Divider dv = make_divider(s);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         float f[8];
         unpack8(v[i], f);
-        const uint2 c = encode8_div(f, dv);
+        const uint2 c = kPow2 ? encode8_mul(f, mul) : encode8_div(f, dv);
         *reinterpret_cast<uint2*>(codes + (n0 + rg * 8 + i) * K + k0 + chunk * 8) = c;
         if (codes_t) *reinterpret_cast<uint2*>(tile + (rg * 8 + i) * kStride + chunk * 8) = c;
     }
@@ -386,28 +438,50 @@ __global__ void __launch_bounds__(256) k_permute_rows_mx(const uint8_t* __restri
 // ---------------------------------------------------------------------------
 // Launchers (argument checks are done by the API layer).
 // ---------------------------------------------------------------------------
+// Padding rows of the last MX atom row (rows >= `rows`) must read as zero.
+cudaError_t zero_mx_tail(void* scales, int64_t rows, int64_t cols, cudaStream_t st) {
+    if (rows % 128 == 0) return cudaSuccess;
+    const int64_t atoms_k = (cols + 127) / 128;
+    return cudaMemsetAsync(static_cast<uint8_t*>(scales) + (rows / 128) * atoms_k * 512, 0, (size_t)atoms_k * 512, st);
+}
+
 cudaError_t launch_quant_group_k(const uint16_t* x, int64_t M, int64_t K, int64_t ld, uint8_t* codes,
-                                 float* scales, cudaStream_t st) {
+                                 void* scales, bool pow2, cudaStream_t st) {
     if (M == 0) return cudaSuccess;
     const int64_t G = K / 128;
     const int64_t blocks = ((M + kGK_Rows - 1) / kGK_Rows) * ((G + kGK_Groups - 1) / kGK_Groups);
-    k_quant_group_k<<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ld, codes, scales);
+    if (pow2) {
+        cudaError_t e = zero_mx_tail(scales, M, K, st);
+        if (e != cudaSuccess) return e;
+        k_quant_group_k<true><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ld, codes, scales);
+    } else {
+        k_quant_group_k<false><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ld, codes, scales);
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_quant_group_m(const uint16_t* x, int64_t M, int64_t K, int64_t ld, uint8_t* codes_t,
-                                 float* scales, cudaStream_t st) {
+                                 void* scales, bool pow2, cudaStream_t st) {
     if (M == 0 || K == 0) return cudaSuccess;
     const int64_t blocks = (M / 128) * ((K + 63) / 64);
-    k_quant_group_m<<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ld, codes_t, scales);
+    if (pow2) {
+        cudaError_t e = zero_mx_tail(scales, K, M, st);  // the output is the [K][M] transpose
+        if (e != cudaSuccess) return e;
+        k_quant_group_m<true><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ld, codes_t, scales);
+    } else {
+        k_quant_group_m<false><<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ld, codes_t, scales);
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_quant_block(const uint16_t* w, int64_t N, int64_t K, int64_t ld, uint8_t* codes,
-                               float* scales, uint8_t* codes_t, float* scales_t, cudaStream_t st) {
+                               void* scales, uint8_t* codes_t, void* scales_t, bool pow2, cudaStream_t st) {
     if (N == 0 || K == 0) return cudaSuccess;
     const int64_t blocks = (N / 128) * (K / 128);
-    k_quant_block<<<(unsigned)blocks, 256, 0, st>>>(w, N, K, ld, codes, scales, codes_t, scales_t);
+    if (pow2)
+        k_quant_block<true><<<(unsigned)blocks, 256, 0, st>>>(w, N, K, ld, codes, scales, codes_t, scales_t);
+    else
+        k_quant_block<false><<<(unsigned)blocks, 256, 0, st>>>(w, N, K, ld, codes, scales, codes_t, scales_t);
     return cudaGetLastError();
 }
 

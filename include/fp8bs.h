@@ -62,7 +62,17 @@ typedef enum {
 
 typedef enum {
     FP8_RECIPE_BLOCKWISE_FP32 = 1, /* fp32 scales: 1x128 / 128x1 groups, 128x128 blocks */
-    FP8_RECIPE_MXFP8 = 2           /* E8M0 scales, 1x32 blocks */
+    FP8_RECIPE_MXFP8 = 2,          /* E8M0 scales, 1x32 blocks */
+    /* The blockwise groups with power-of-two scales ([SkyRL] "Deep dive:
+     * FP8 quantization with FP32 and power-of-two block scales": Blackwell
+     * tensor cores take only power-of-two block scales).  Scale 2^e with
+     * e = ceil(log2(amax/448)) (amax/448 the fp32 recipe's IEEE quotient),
+     * clamped to [-127, 127], e = 0 for an all-zero group; codes from the
+     * exact product x * 2^-e.  Scales are E8M0 bytes (e + 127) in
+     * FP8_LAYOUT_MX_1x32, each group's byte repeated in the 1x32 blocks it
+     * covers, so the tensor is also a valid MXFP8 tensor and the GEMMs run
+     * on the block-scaled MMA with no promotion. */
+    FP8_RECIPE_BLOCKWISE_POW2 = 3
 } fp8_recipe;
 
 typedef enum {
@@ -125,6 +135,10 @@ typedef struct {
 /* ---------------------------------------------------------------------- */
 
 /* Group quantization of a bf16 matrix x [M][ld] (first K columns used).
+ * out->recipe selects the scales: FP8_RECIPE_BLOCKWISE_FP32 with the fp32
+ * layouts below, or FP8_RECIPE_BLOCKWISE_POW2 with out->layout =
+ * FP8_LAYOUT_MX_1x32 and a scale buffer of fp8_mx_scale_bytes(rows, cols)
+ * of the output (K x M for FP8_AXIS_M); the codes are laid out the same.
  * [Jet-RL] "Kwantisatieschema": activations in 1x128 groups; for WGrad the
  * operands in 128x1 groups.  [AIS] equation Q(X): s = max|X| / qmax.
  *  axis = FP8_AXIS_K: out->codes [M][K], out->scales fp32 [K/128][M];
@@ -134,7 +148,8 @@ typedef struct {
  *                     [M/128][K] -- exactly the 1x128 quantization of x^T.
  *                     Requires M % 128 == 0, K % 8 == 0.
  * out->rows/cols must equal (M, K) for AXIS_K and (K, M) for AXIS_M;
- * out->recipe = FP8_RECIPE_BLOCKWISE_FP32, out->layout = FP8_LAYOUT_GROUP_1x128. */
+ * out->recipe = FP8_RECIPE_BLOCKWISE_FP32, out->layout = FP8_LAYOUT_GROUP_1x128
+ * (or FP8_RECIPE_BLOCKWISE_POW2 with FP8_LAYOUT_MX_1x32). */
 fp8_status fp8_quantize_group(const void* x_bf16, int64_t M, int64_t K, int64_t ld,
                               fp8_axis axis, const fp8_tensor* out, fp8_stream_t stream);
 
@@ -145,7 +160,9 @@ fp8_status fp8_quantize_group(const void* x_bf16, int64_t M, int64_t K, int64_t 
  * out_t (nullable): the same codes transposed [K][N] with the transposed
  * scale grid [K/128][N/128] (rows = K, cols = N), the DGrad B operand;
  * [SkyRL] "Performance analysis", トレーニング: the trainer keeps a row-wise and a
- * transposed copy. */
+ * transposed copy.  FP8_RECIPE_BLOCKWISE_POW2 in out (and out_t):
+ * power-of-two scales in FP8_LAYOUT_MX_1x32 instead, every byte of a block's
+ * 512-byte atom holding its exponent. */
 fp8_status fp8_quantize_block(const void* w_bf16, int64_t N, int64_t K, int64_t ld,
                               const fp8_tensor* out, const fp8_tensor* out_t,
                               fp8_stream_t stream);
@@ -193,6 +210,10 @@ fp8_status fp8_permute_rows_mx(const fp8_tensor* src, const int32_t* gather_dev,
  *  MXFP8 recipe ([SkyRL] "Performance analysis": fp8_recipe=auto selects native
  *  MXFP8 on Blackwell): D = sum_k qa 2^ea(m,k/32) qb 2^eb(n,k/32); A and B
  *  in layout MX_1x32; op must be FP8_GEMM_FWD.
+ *  Blockwise recipe with power-of-two scales (both operands
+ *  FP8_RECIPE_BLOCKWISE_POW2, layout MX_1x32): the blockwise formula with
+ *  sa, sb powers of two, computed by the block-scaled MMA; FWD, DGRAD and
+ *  WGRAD (operands as for the fp32 recipe); bf16 D only.
  * Sizes: M = A->rows, K = A->cols = B->cols, N = B->rows.  K % 128 == 0,
  * N % 16 == 0 (blockwise: N % 128 == 0), any M >= 0.
  * D: [M][ldd] of d_dtype (FP8_OUT_F32 only for the blockwise recipe).
@@ -200,7 +221,9 @@ fp8_status fp8_permute_rows_mx(const fp8_tensor* src, const int32_t* gather_dev,
  * inside the epilogue ([SkyRL] "Performance analysis", 生成: activation quantization folded into
  * the GEMM kernel; [Jet-RL] "Kwantisatieschema": fused with the previous
  * operator): blockwise -> 1x128 groups (GROUP_1x128, N % 128 == 0);
- * MXFP8 -> 1x32 (MX_1x32).  d_quant rows/cols = (M, N); requires bf16 D.
+ * MXFP8 -> 1x32 (MX_1x32); power-of-two blockwise -> 1x128 groups with
+ * power-of-two scales (MX_1x32, N % 128 == 0).  d_quant rows/cols =
+ * (M, N); requires bf16 D.
  * The result equals fp8_quantize_group / fp8_quantize_mx applied to D. */
 fp8_status fp8_gemm_blockscaled(const fp8_tensor* A, const fp8_tensor* B, void* D, int64_t ldd,
                                 int32_t d_dtype, int32_t op, const fp8_tensor* d_quant,

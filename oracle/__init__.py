@@ -274,7 +274,7 @@ class _Entry(C.Structure):
 
 
 KIND_FP8, KIND_BF16 = 1, 2
-RECIPE_NONE, RECIPE_BLOCKWISE, RECIPE_MX = 0, 1, 2
+RECIPE_NONE, RECIPE_BLOCKWISE, RECIPE_MX, RECIPE_BLOCKWISE_POW2 = 0, 1, 2, 3
 LAYOUT_NONE, LAYOUT_GROUP_1x128, LAYOUT_BLOCK_128x128, LAYOUT_MX_1x32 = 0, 1, 2, 3
 
 
