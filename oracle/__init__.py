@@ -41,6 +41,7 @@ def load():
         "oracle_mx_scale_offset": (_I64, [_I64, _I64, _I64]),
         "oracle_mx_scale_bytes": (_I64, [_I64, _I64]),
         "oracle_quant_mx_1x32": (None, [_P, _I64, _I64, _I64, _P, _P]),
+        "oracle_quant_mx_32x1_T": (None, [_P, _I64, _I64, _I64, _P, _P]),
         "oracle_pow2_exponent": (C.c_int, [C.c_float]),
         "oracle_quant_group_1x128_pow2": (None, [_P, _I64, _I64, _I64, _P, _P]),
         "oracle_quant_group_128x1_T_pow2": (None, [_P, _I64, _I64, _I64, _P, _P]),
@@ -146,6 +147,16 @@ def quant_mx_1x32(x_bits):
     scales = np.empty((mx_scale_bytes(R, K),), np.uint8)
     load().oracle_quant_mx_1x32(_ptr(x), R, K, K, _ptr(codes), _ptr(scales))
     return codes, scales
+
+
+def quant_mx_32x1_T(x_bits):
+    """32x1 MX blocks along the rows, codes transposed [K][R] (MX backward)."""
+    x = _bits(x_bits)
+    R, K = x.shape
+    codes_t = np.empty((K, R), np.uint8)
+    scales_t = np.empty((mx_scale_bytes(K, R),), np.uint8)
+    load().oracle_quant_mx_32x1_T(_ptr(x), R, K, K, _ptr(codes_t), _ptr(scales_t))
+    return codes_t, scales_t
 
 
 def pow2_exponent(amax: float) -> int:

@@ -352,6 +352,33 @@ void oracle_quant_mx_1x32(const uint16_t* x, int64_t R, int64_t K, int64_t ld,
     }
 }
 
+/* 32x1 blocks along the rows, codes written transposed: the MXFP8 backward
+ * operands (WGrad contracts over the token dimension M, DGrad's B operand is
+ * W^T) -- exactly oracle_quant_mx_1x32 of x^T.  x: bf16 [R][ld];
+ * codesT [K][R]; scalesT: MX atoms of the [K][R] tensor. */
+void oracle_quant_mx_32x1_T(const uint16_t* x, int64_t R, int64_t K, int64_t ld,
+                            uint8_t* codesT, uint8_t* scalesT)
+{
+    memset(scalesT, 0, (size_t)oracle_mx_scale_bytes(K, R));
+    int64_t RB = R / 32;
+    #pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < K; ++c) {
+        for (int64_t rb = 0; rb < RB; ++rb) {
+            float amax = 0.0f;
+            for (int64_t i = 0; i < 32; ++i) {
+                float a = fabsf(bf16_bits_to_f32(x[(rb * 32 + i) * ld + c]));
+                if (a > amax) amax = a;
+            }
+            int e = mx_exponent(amax);
+            scalesT[oracle_mx_scale_offset(c, rb, R)] = (uint8_t)(e + 127);
+            for (int64_t i = 0; i < 32; ++i) {
+                double v = ldexp((double)bf16_bits_to_f32(x[(rb * 32 + i) * ld + c]), -e);
+                codesT[c * R + rb * 32 + i] = oracle_e4m3_encode_f64(v);
+            }
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Blockwise recipe with power-of-two scales ([P1] "Deep dive: FP8            */
 /* quantization with FP32 and power-of-two block scales": Blackwell's tensor  */

@@ -247,3 +247,28 @@ def test_mx_zero_block_and_padding(orc):
     assert scales[orc.mx_scale_offset(1, 1, 64)] == 127 + (1 - 8)
     assert codes[1, 40] == 0xF8                                  # -2 * 2^7 = -256
     assert np.count_nonzero(codes) == 1
+
+
+# ---------------------------------------------------------------- MX backward operands
+def test_mx_32x1_transposed_is_the_1x32_quantization_of_the_transpose(orc):
+    x = synth.random_bf16((256, 200), seed=21, outliers=True)
+    bits = synth.bf16_bits(x)
+    ct, st = orc.quant_mx_32x1_T(bits)
+    c2, s2 = orc.quant_mx_1x32(np.ascontiguousarray(bits.T))
+    assert ct.shape == (200, 256)
+    assert np.array_equal(ct, c2)
+    assert np.array_equal(st, s2)
+
+
+def test_mx_32x1_block_exponent_brute_force(orc):
+    # one column: 32-row blocks with known maxima; e = floor(log2 amax) - 8
+    x = np.zeros((64, 32), np.float32)
+    x[:32, 0] = np.linspace(-3.0, 3.0, 32)      # amax 3 -> e = 1 - 8 = -7
+    x[32:, 0] = 1.0                              # amax 1 -> e = -8
+    ct, st = orc.quant_mx_32x1_T(_bits_of(x))
+    assert st[orc.mx_scale_offset(0, 0, 64)] == 127 - 7
+    assert st[orc.mx_scale_offset(0, 1, 64)] == 127 - 8
+    v = synth.bf16_bits(torch.tensor(x).to(torch.bfloat16))
+    vals = (v.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.array_equal(ct[0, :32], _brute_force_encode(vals[:32, 0] * 2.0 ** 7))
+    assert np.array_equal(ct[0, 32:], _brute_force_encode(vals[32:, 0] * 2.0 ** 8))
