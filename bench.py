@@ -261,7 +261,18 @@ def breakdown(fp8, synth, dev, flush, pk, reps):
     dW = torch.empty((Nb, Kb), dtype=torch.bfloat16, device=dev)
     rec("gemm_blockwise_wgrad", time_kernel(lambda: fp8.gemm(q_dyt, q_xt, "wgrad", out=dW), flush, reps),
         flops=2.0 * Mb * Nb * Kb, workload="dW = dY^T X, 4096x8192(M)x4096")
-    del dY, Wb, Xb, q_dy, q_w, q_wt, q_dyt, q_xt, dX, dW
+    # the same backward in MXFP8: 32x1 blocks for the transposed operands
+    m_dy = fp8.quantize_mx(dY)
+    m_wt = fp8.quantize_mx(Wb, transposed=True)
+    m_dyt = fp8.quantize_mx(dY, transposed=True)
+    m_xt = fp8.quantize_mx(Xb, transposed=True)
+    rec("quant_mx_32x1_T", time_kernel(lambda: fp8.quantize_mx(Xb, out=m_xt, transposed=True), flush, reps),
+        bytes_=Mb * Kb * (3 + 1 / 32), workload="X 8192x4096 -> X^T, 32x1 blocks")
+    rec("gemm_mx_dgrad", time_kernel(lambda: fp8.gemm(m_dy, m_wt, "dgrad", out=dX), flush, reps),
+        flops=2.0 * Mb * Nb * Kb, workload="MXFP8 dX = dY W, 8192x4096(N)x4096")
+    rec("gemm_mx_wgrad", time_kernel(lambda: fp8.gemm(m_dyt, m_xt, "wgrad", out=dW), flush, reps),
+        flops=2.0 * Mb * Nb * Kb, workload="MXFP8 dW = dY^T X, 4096x8192(M)x4096")
+    del dY, Wb, Xb, q_dy, q_w, q_wt, q_dyt, q_xt, dX, dW, m_dy, m_wt, m_dyt, m_xt
     torch.cuda.empty_cache()
 
     # MXFP8 forward
@@ -307,15 +318,19 @@ def _case_gemm(kind):
             if kind in ("fwd", "pow2"):
                 return lambda: fp8.gemm(qx, qw, out=Y), 2.0 * M * N * K
             return lambda: fp8.gemm(qx, qw, quantize_output=True, out=Y, out_q=qy), 2.0 * M * N * K
-        if kind in ("dgrad", "wgrad"):
+        if kind in ("dgrad", "wgrad", "mx_dgrad", "mx_wgrad"):
             wl = synth.backward()
             dY, W, X = (wl.tensors[k].to(dev) for k in ("dY", "W", "X"))
-            if kind == "dgrad":
+            if kind == "mx_dgrad":
+                a, b = fp8.quantize_mx(dY), fp8.quantize_mx(W, transposed=True)
+            elif kind == "mx_wgrad":
+                a, b = fp8.quantize_mx(dY, transposed=True), fp8.quantize_mx(X, transposed=True)
+            elif kind == "dgrad":
                 a, (_, b) = fp8.quantize_group(dY, "K"), fp8.quantize_block(W, True)
             else:
                 a, b = fp8.quantize_group(dY, "M"), fp8.quantize_group(X, "M")
             D = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=dev)
-            return lambda: fp8.gemm(a, b, kind, out=D), 2.0 * 8192 * 4096 * 4096
+            return lambda: fp8.gemm(a, b, kind.replace("mx_", ""), out=D), 2.0 * 8192 * 4096 * 4096
         if kind == "mx":
             wl = synth.mx()
             a, b = fp8.quantize_mx(wl.tensors["X"].to(dev)), fp8.quantize_mx(wl.tensors["W"].to(dev))
@@ -346,6 +361,10 @@ def _case_quant(kind):
             X = synth.backward().tensors["X"].to(dev)
             q = fp8.quantize_group(X, "M")
             return lambda: fp8.quantize_group(X, "M", out=q), None
+        if kind == "mx_t":
+            X = synth.backward().tensors["X"].to(dev)
+            q = fp8.quantize_mx(X, transposed=True)
+            return lambda: fp8.quantize_mx(X, out=q, transposed=True), None
         W = synth.mx().tensors["W"].to(dev)
         q = fp8.quantize_mx(W)
         return lambda: fp8.quantize_mx(W, out=q), None
@@ -359,6 +378,8 @@ KERNEL_CASES = {
     "gemm_blockwise_pow2_fwd": _case_gemm("pow2"), "gemm_blockwise_pow2_fwd_fused": _case_gemm("pow2_fused"),
     "quant_group_1x128": _case_quant("group_k"), "quant_block_128x128": _case_quant("block"),
     "quant_group_128x1_T": _case_quant("group_m"), "quant_mx_1x32": _case_quant("mx"),
+    "gemm_mx_dgrad": _case_gemm("mx_dgrad"), "gemm_mx_wgrad": _case_gemm("mx_wgrad"),
+    "quant_mx_32x1_T": _case_quant("mx_t"),
 }
 
 

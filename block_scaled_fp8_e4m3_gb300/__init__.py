@@ -73,6 +73,7 @@ def library() -> C.CDLL:
         "fp8_quantize_group": [P, I64, I64, I64, I32, TP, S],
         "fp8_quantize_block": [P, I64, I64, I64, TP, TP, S],
         "fp8_quantize_mx": [P, I64, I64, I64, TP, S],
+        "fp8_quantize_mx_transposed": [P, I64, I64, I64, TP, S],
         "fp8_permute_rows_mx": [TP, P, P, I32, TP, S],
         "fp8_gemm_blockscaled": [TP, TP, P, I64, I32, I32, TP, S],
         "fp8_grouped_gemm": [TP, TP, P, I32, I64, P, I64, S],
@@ -199,11 +200,20 @@ def quantize_block(w: torch.Tensor, transposed: bool = False, out: Optional[QTen
     return (q, qt) if transposed else q
 
 
-def quantize_mx(x: torch.Tensor, out: Optional[QTensor] = None, stream=None) -> QTensor:
-    """MXFP8: 1x32 blocks, E8M0 scales in the tensor-core atom layout."""
+def quantize_mx(x: torch.Tensor, out: Optional[QTensor] = None, stream=None, transposed: bool = False) -> QTensor:
+    """MXFP8: 1x32 blocks, E8M0 scales in the tensor-core atom layout.
+    transposed=True: 32x1 blocks along the rows, codes written transposed
+    [K, R] (the MXFP8 backward operands W^T, dY^T, X^T)."""
     x = _bf16_2d(x)
     R, K = x.shape
     dev = _dev(x)
+    if transposed:
+        q = out or QTensor(torch.empty((K, R), dtype=torch.uint8, device=dev),
+                           torch.empty((mx_scale_bytes(K, R),), dtype=torch.uint8, device=dev), K, R, RECIPE_MX,
+                           LAYOUT_MX_1x32)
+        t = q.c()
+        _check(library().fp8_quantize_mx_transposed(x.data_ptr(), R, K, x.stride(0), C.byref(t), _stream(stream)))
+        return q
     q = out or QTensor(torch.empty((R, K), dtype=torch.uint8, device=dev),
                 torch.empty((mx_scale_bytes(R, K),), dtype=torch.uint8, device=dev), R, K, RECIPE_MX,
                 LAYOUT_MX_1x32)

@@ -399,6 +399,20 @@ fp8_status fp8_quantize_mx(const void* x_bf16, int64_t R, int64_t K, int64_t ld,
     return e == cudaSuccess ? FP8_OK : cuda_fail(e, "quantize_mx");
 }
 
+fp8_status fp8_quantize_mx_transposed(const void* x_bf16, int64_t R, int64_t K, int64_t ld, const fp8_tensor* out,
+                                      fp8_stream_t stream) {
+    fp8_status s = check_input(x_bf16, R, K, ld, "x");
+    if (s != FP8_OK) return s;
+    if (R % 128 != 0 || K % 8 != 0)
+        return fail(FP8_ERR_UNSUPPORTED, "32x1 blocks need R %% 128 == 0 and K %% 8 == 0 (R = %lld, K = %lld)",
+                    (long long)R, (long long)K);
+    s = check_out(out, "out", FP8_RECIPE_MXFP8, FP8_LAYOUT_MX_1x32, K, R);
+    if (s != FP8_OK) return s;
+    cudaError_t e = launch_quant_mx_t(static_cast<const uint16_t*>(x_bf16), R, K, ld, static_cast<uint8_t*>(out->codes),
+                                      static_cast<uint8_t*>(out->scales), reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : cuda_fail(e, "quantize_mx_transposed");
+}
+
 fp8_status fp8_permute_rows_mx(const fp8_tensor* src, const int32_t* gather_dev, const int32_t* m_offsets_dev,
                                int32_t num_groups, const fp8_tensor* dst, fp8_stream_t stream) {
     if (src == nullptr || dst == nullptr || gather_dev == nullptr || m_offsets_dev == nullptr)
@@ -488,7 +502,6 @@ fp8_status fp8_gemm_blockscaled(const fp8_tensor* A, const fp8_tensor* B, void* 
         // recipe's scales are MX scales constant over each group
         const int recipe = A->recipe;
         const bool pow2 = recipe == FP8_RECIPE_BLOCKWISE_POW2;
-        if (!pow2 && op != FP8_GEMM_FWD) return fail(FP8_ERR_UNSUPPORTED, "MXFP8 GEMM supports FP8_GEMM_FWD only");
         if (op != FP8_GEMM_FWD && op != FP8_GEMM_DGRAD && op != FP8_GEMM_WGRAD)
             return fail(FP8_ERR_INVALID_ARG, "unknown op %d", op);
         if (d_dtype != FP8_OUT_BF16) return fail(FP8_ERR_UNSUPPORTED, "this recipe's GEMM writes bf16 only");

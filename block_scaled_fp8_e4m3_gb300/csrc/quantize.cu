@@ -387,6 +387,86 @@ __global__ void __launch_bounds__(256) k_quant_mx(const uint16_t* __restrict__ x
 }
 
 // ---------------------------------------------------------------------------
+// MX 32x1 blocks along the rows, codes transposed (the MXFP8 backward
+// operands: W^T for DGrad, dY^T and X^T for WGrad) -- the 1x32 quantization
+// of x^T.  Block = one 128-row x 64-column tile; thread (chunk = t%8,
+// quad = t/8) holds rows 4*quad..4*quad+3 of columns 8*chunk..8*chunk+7, so a
+// warp covers 16 rows and a 32-row block is two warps.  Block maxima: in
+// thread over 4 rows, shuffles over the warp's 4 quads, shared memory over
+// the warp pair; one 32-bit store per column carries the 4 exponents of its
+// 128 rows.  Codes are the exact products x * 2^-e, transposed through a
+// 33-word-stride shared tile and written 16 bytes per thread.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_quant_mx_t(const uint16_t* __restrict__ x, int64_t R, int64_t K,
+                                                    int64_t ld, uint8_t* __restrict__ codes_t,
+                                                    uint8_t* __restrict__ scales_t) {
+    __shared__ float red[8][64];
+    __shared__ float col_mul[4][64];
+    __shared__ uint32_t tile[64 * 33];
+
+    const int64_t ctiles = (K + 63) / 64;
+    const int64_t mb = (int64_t)blockIdx.x / ctiles;
+    const int64_t c0 = ((int64_t)blockIdx.x % ctiles) * 64;
+    const int64_t m0 = mb * 128;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int chunk = t & 7, quad = t >> 3;
+    const bool col_ok = c0 + chunk * 8 < K;  // K % 8 == 0: a chunk is all valid or all invalid
+
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        v[i] = col_ok ? ld_stream_v4(x + (m0 + quad * 4 + i) * ld + c0 + chunk * 8) : make_uint4(0, 0, 0, 0);
+    float f[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) unpack8(v[i], f[i]);
+    float pa[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float a = fmaxf(fmaxf(fabsf(f[0][j]), fabsf(f[1][j])), fmaxf(fabsf(f[2][j]), fabsf(f[3][j])));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
+        pa[j] = a;
+    }
+    if (lane < 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) red[warp][chunk * 8 + j] = pa[j];
+    }
+    __syncthreads();
+    if (t < 64) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int e = mx_exponent(fmaxf(red[2 * b][t], red[2 * b + 1][t]));
+            col_mul[b][t] = exp2_int(-e);
+            word |= (uint32_t)(e + 127) << (8 * b);
+        }
+        // transposed row c0+t, 1x32 blocks 4mb..4mb+3 of the [K][R] output
+        if (c0 + t < K) *reinterpret_cast<uint32_t*>(scales_t + mx_scale_offset(c0 + t, 4 * mb, R / 128)) = word;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float mul = col_mul[warp >> 1][chunk * 8 + j];
+        tile[(chunk * 8 + j) * 33 + quad] = e4m3x2(__fmul_rn(f[0][j], mul), __fmul_rn(f[1][j], mul)) |
+                                            (e4m3x2(__fmul_rn(f[2][j], mul), __fmul_rn(f[3][j], mul)) << 16);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int idx = t + 256 * i;
+        const int col = idx >> 3, part = idx & 7;
+        if (c0 + col < K) {
+            uint4 o;
+            o.x = tile[col * 33 + part * 4 + 0];
+            o.y = tile[col * 33 + part * 4 + 1];
+            o.z = tile[col * 33 + part * 4 + 2];
+            o.w = tile[col * 33 + part * 4 + 3];
+            *reinterpret_cast<uint4*>(codes_t + (c0 + col) * R + m0 + part * 16) = o;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // MoE row gather of MX codes and scales into expert-contiguous groups.  One
 // warp per destination row: 16-byte code copies, then one 32-bit word per
 // 128-column atom (the 4 scale bytes of a row inside an atom are adjacent).
@@ -490,6 +570,16 @@ cudaError_t launch_quant_mx(const uint16_t* x, int64_t R, int64_t K, int64_t ld,
     if (R == 0 || K == 0) return cudaSuccess;
     const int64_t blocks = ((R + 127) / 128) * ((K + 127) / 128);
     k_quant_mx<<<(unsigned)blocks, 256, 0, st>>>(x, R, K, ld, codes, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_mx_t(const uint16_t* x, int64_t R, int64_t K, int64_t ld, uint8_t* codes_t,
+                              uint8_t* scales_t, cudaStream_t st) {
+    if (R == 0 || K == 0) return cudaSuccess;
+    cudaError_t e = zero_mx_tail(scales_t, K, R, st);  // the output is the [K][R] transpose
+    if (e != cudaSuccess) return e;
+    const int64_t blocks = (R / 128) * ((K + 63) / 64);
+    k_quant_mx_t<<<(unsigned)blocks, 256, 0, st>>>(x, R, K, ld, codes_t, scales_t);
     return cudaGetLastError();
 }
 

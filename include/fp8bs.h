@@ -177,6 +177,15 @@ fp8_status fp8_quantize_block(const void* w_bf16, int64_t N, int64_t K, int64_t 
 fp8_status fp8_quantize_mx(const void* x_bf16, int64_t R, int64_t K, int64_t ld,
                            const fp8_tensor* out, fp8_stream_t stream);
 
+/* MXFP8 operands of the backward GEMMs: 32x1 blocks along the rows of x
+ * [R][ld] (first K columns), codes written transposed -- exactly the 1x32
+ * quantization of x^T.  out: codes [K][R], scales FP8_LAYOUT_MX_1x32 of the
+ * K x R output (fp8_mx_scale_bytes(K, R) bytes); out->rows/cols = (K, R),
+ * recipe FP8_RECIPE_MXFP8.  Requires R % 128 == 0, K % 8 == 0.  DGrad:
+ * B = W^T from W [N][K]; WGrad: A = dY^T, B = X^T. */
+fp8_status fp8_quantize_mx_transposed(const void* x_bf16, int64_t R, int64_t K, int64_t ld,
+                                      const fp8_tensor* out, fp8_stream_t stream);
+
 /* Bytes of an FP8_LAYOUT_MX_1x32 scale buffer for a rows x cols matrix. */
 int64_t fp8_mx_scale_bytes(int64_t rows, int64_t cols);
 /* Upper bound of an FP8_LAYOUT_MX_1x32_GROUPED scale buffer. */
@@ -209,7 +218,8 @@ fp8_status fp8_permute_rows_mx(const fp8_tensor* src, const int32_t* gather_dev,
  *    for WGRAD (its 128x1 scales become per-column scales of D).
  *  MXFP8 recipe ([SkyRL] "Performance analysis": fp8_recipe=auto selects native
  *  MXFP8 on Blackwell): D = sum_k qa 2^ea(m,k/32) qb 2^eb(n,k/32); A and B
- *  in layout MX_1x32; op must be FP8_GEMM_FWD.
+ *  in layout MX_1x32; FWD, DGRAD (B = W^T from fp8_quantize_mx_transposed)
+ *  and WGRAD (A = dY^T, B = X^T, both from fp8_quantize_mx_transposed).
  *  Blockwise recipe with power-of-two scales (both operands
  *  FP8_RECIPE_BLOCKWISE_POW2, layout MX_1x32): the blockwise formula with
  *  sa, sb powers of two, computed by the block-scaled MMA; FWD, DGRAD and

@@ -51,6 +51,7 @@ def _t(rows, cols, recipe, layout, codes=0x10000, scales=0x20000):
     ("group_k_bad_K", 3), ("group_m_bad_M", 3), ("block_bad_N", 3), ("mx_bad_K", 3),
     ("misaligned", 2), ("bad_ld", 1), ("wrong_layout", 1), ("wrong_shape", 1), ("null_out", 1),
     ("gemm_bad_K", 3), ("gemm_K_mismatch", 1), ("gemm_bad_N", 3),
+    ("mx_t_bad_R", 3), ("mx_t_wrong_shape", 1),
 ])
 def test_argument_validation_happens_on_host(lib, case, expect):
     x = 0x100000                                   # never dereferenced: validation fails first
@@ -67,6 +68,12 @@ def test_argument_validation_happens_on_host(lib, case, expect):
     elif case == "mx_bad_K":
         t = _t(4, 40, 2, 3)
         st = lib.fp8_quantize_mx(x, 4, 40, 40, C.byref(t), s)
+    elif case == "mx_t_bad_R":
+        t = _t(64, 100, 2, 3)
+        st = lib.fp8_quantize_mx_transposed(x, 100, 64, 64, C.byref(t), s)
+    elif case == "mx_t_wrong_shape":
+        t = _t(128, 64, 2, 3)                      # must be (K, R) = (64, 128)
+        st = lib.fp8_quantize_mx_transposed(x, 128, 64, 64, C.byref(t), s)
     elif case == "misaligned":
         t = _t(4, 128, 1, 1)
         st = lib.fp8_quantize_group(x + 2, 4, 128, 128, 0, C.byref(t), s)
