@@ -46,6 +46,9 @@ def load():
         "oracle_quant_group_1x128_pow2": (None, [_P, _I64, _I64, _I64, _P, _P]),
         "oracle_quant_group_128x1_T_pow2": (None, [_P, _I64, _I64, _I64, _P, _P]),
         "oracle_quant_block_128x128_pow2": (None, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
+        "oracle_param_update": (None, [_P, _P, _I64, _I64, _I64]),
+        "oracle_quant_block_128x128_f32": (None, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
+        "oracle_quant_block_128x128_f32_pow2": (None, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
         "oracle_dequant_group": (None, [_P, _P, _I64, _I64, _P]),
         "oracle_dequant_block": (None, [_P, _P, _I64, _I64, _P]),
         "oracle_dequant_mx": (None, [_P, _P, _I64, _I64, _P]),
@@ -194,6 +197,45 @@ def quant_block_128x128_pow2(w_bits, transposed: bool = False):
                                                _ptr(codes_t), _ptr(scales_t))
         return codes, scales, codes_t, scales_t
     load().oracle_quant_block_128x128_pow2(_ptr(w), N, K, K, _ptr(codes), _ptr(scales), None, None)
+    return codes, scales
+
+
+# ---------------------------------------------------------------- fp8_param
+def _f32(x) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.float32:
+        raise TypeError("fp32 master weights are passed as float32 arrays")
+    return x
+
+
+def param_update(master, delta) -> np.ndarray:
+    """W_t = W_{t-1} + dW in fp32 (returns a new array)."""
+    m = _f32(master).copy()
+    d = _f32(delta)
+    assert m.shape == d.shape and m.ndim == 2
+    load().oracle_param_update(_ptr(m), _ptr(d), m.shape[0], m.shape[1], m.shape[1])
+    return m
+
+
+def quant_block_128x128_f32(w, transposed: bool = False, pow2: bool = False):
+    """Q(W) of an fp32 master: 128x128 blocks, fp32 scales [N/128][K/128] or
+    (pow2) E8M0 bytes in the MX atom layout."""
+    w = _f32(w)
+    N, K = w.shape
+    codes = np.empty((N, K), np.uint8)
+    if pow2:
+        scales = np.empty((mx_scale_bytes(N, K),), np.uint8)
+        scales_t = np.empty((mx_scale_bytes(K, N),), np.uint8) if transposed else None
+        fn = load().oracle_quant_block_128x128_f32_pow2
+    else:
+        scales = np.empty((N // 128, K // 128), np.float32)
+        scales_t = np.empty((K // 128, N // 128), np.float32) if transposed else None
+        fn = load().oracle_quant_block_128x128_f32
+    codes_t = np.empty((K, N), np.uint8) if transposed else None
+    fn(_ptr(w), N, K, K, _ptr(codes), _ptr(scales),
+       _ptr(codes_t) if transposed else None, _ptr(scales_t) if transposed else None)
+    if transposed:
+        return codes, scales, codes_t, scales_t
     return codes, scales
 
 

@@ -182,12 +182,15 @@ void oracle_e4m3_decode_array(const uint8_t* c, int64_t n, double* out)
 /* ------------------------------------------------------------------------ */
 
 /* Scale of one group: s = amax / 448 in fp32 ([P2] eq. Q(X) with the E4M3
- * maximum in place of 2^(b-1)-1); s = 1 for an all-zero group. */
+ * maximum in place of 2^(b-1)-1); s = 1 for an all-zero group, and likewise
+ * when the quotient underflows to 0 (amax below 448 * 2^-150, reachable only
+ * with fp32 inputs), so that no block divides by zero. */
 static float group_scale(float amax)
 {
-    if (amax == 0.0f)
+    float s = amax / 448.0f;
+    if (s == 0.0f)
         return 1.0f;
-    return amax / 448.0f;
+    return s;
 }
 
 static uint8_t encode_div(float x, float s)
@@ -487,6 +490,92 @@ void oracle_quant_block_128x128_pow2(const uint16_t* w, int64_t N, int64_t K, in
                 for (int64_t j = 0; j < 128; ++j) {
                     int64_t n = nb * 128 + i, k = kb * 128 + j;
                     uint8_t q = encode_pow2(bf16_bits_to_f32(w[n * ld + k]), e);
+                    codes[n * K + k] = q;
+                    if (codesT) codesT[k * N + n] = q;
+                }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* fp8_param ([P1] overview: FP8 parameters plus an FP32 master, no BF16     */
+/* copy; "Deep dive: FP8 quantization with FP32 and power-of-two block       */
+/* scales": the optimizer updates the FP32 master and, after every step, the */
+/* FP8 storage is recomputed from it as Q(W_t)).  The update is the add that */
+/* ends an optimizer step, W_t = W_{t-1} + dW in fp32; Q is the 128x128      */
+/* block quantizer of either recipe applied to the fp32 values themselves    */
+/* (no bf16 rounding in between).                                            */
+/* ------------------------------------------------------------------------ */
+
+/* master[n][k] += delta[n][k] (one IEEE fp32 addition each); both [N][ld]. */
+void oracle_param_update(float* master, const float* delta, int64_t N, int64_t K, int64_t ld)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            master[n * ld + k] = master[n * ld + k] + delta[n * ld + k];
+}
+
+/* fp32 scales: as oracle_quant_block_128x128 with fp32 inputs: s =
+ * RN(amax / 448) (1 for an all-zero block), codes = E4M3(RN(w / s)).
+ * w: fp32 [N][ld]; codes [N][K], scales [N/128][K/128]; optional transposed
+ * copy codesT [K][N], scalesT [K/128][N/128]. */
+void oracle_quant_block_128x128_f32(const float* w, int64_t N, int64_t K, int64_t ld,
+                                    uint8_t* codes, float* scales,
+                                    uint8_t* codesT, float* scalesT)
+{
+    int64_t NB = N / 128, KB = K / 128;
+    #pragma omp parallel for schedule(static)
+    for (int64_t nb = 0; nb < NB; ++nb) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            float amax = 0.0f;
+            for (int64_t i = 0; i < 128; ++i)
+                for (int64_t j = 0; j < 128; ++j) {
+                    float a = fabsf(w[(nb * 128 + i) * ld + kb * 128 + j]);
+                    if (a > amax) amax = a;
+                }
+            float s = group_scale(amax);
+            scales[nb * KB + kb] = s;
+            if (scalesT) scalesT[kb * NB + nb] = s;
+            for (int64_t i = 0; i < 128; ++i)
+                for (int64_t j = 0; j < 128; ++j) {
+                    int64_t n = nb * 128 + i, k = kb * 128 + j;
+                    uint8_t q = encode_div(w[n * ld + k], s);
+                    codes[n * K + k] = q;
+                    if (codesT) codesT[k * N + n] = q;
+                }
+        }
+    }
+}
+
+/* Power-of-two scales: as oracle_quant_block_128x128_pow2 with fp32 inputs
+ * (e from the fp32 recipe's scale of the block maximum, codes from the exact
+ * w * 2^-e, E8M0 bytes in the MX atom layout). */
+void oracle_quant_block_128x128_f32_pow2(const float* w, int64_t N, int64_t K, int64_t ld,
+                                         uint8_t* codes, uint8_t* scales,
+                                         uint8_t* codesT, uint8_t* scalesT)
+{
+    memset(scales, 0, (size_t)oracle_mx_scale_bytes(N, K));
+    if (scalesT) memset(scalesT, 0, (size_t)oracle_mx_scale_bytes(K, N));
+    int64_t NB = N / 128, KB = K / 128;
+    #pragma omp parallel for schedule(static)
+    for (int64_t nb = 0; nb < NB; ++nb) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            float amax = 0.0f;
+            for (int64_t i = 0; i < 128; ++i)
+                for (int64_t j = 0; j < 128; ++j) {
+                    float a = fabsf(w[(nb * 128 + i) * ld + kb * 128 + j]);
+                    if (a > amax) amax = a;
+                }
+            int e = oracle_pow2_exponent(amax);
+            for (int64_t i = 0; i < 128; ++i)
+                for (int64_t q = 0; q < 4; ++q) {
+                    scales[oracle_mx_scale_offset(nb * 128 + i, 4 * kb + q, K)] = (uint8_t)(e + 127);
+                    if (scalesT) scalesT[oracle_mx_scale_offset(kb * 128 + i, 4 * nb + q, N)] = (uint8_t)(e + 127);
+                }
+            for (int64_t i = 0; i < 128; ++i)
+                for (int64_t j = 0; j < 128; ++j) {
+                    int64_t n = nb * 128 + i, k = kb * 128 + j;
+                    uint8_t q = encode_pow2(w[n * ld + k], e);
                     codes[n * K + k] = q;
                     if (codesT) codesT[k * N + n] = q;
                 }
