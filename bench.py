@@ -242,6 +242,22 @@ def breakdown(fp8, synth, dev, flush, pk, reps):
     del X, W, qx, qw, Y, Y2, qy, payload, rollout, px, pw, Y3, qy3
     torch.cuda.empty_cache()
 
+    # fp8_param: Q(W) of the fp32 master, alone and fused with the update
+    wl = synth.fp8_param()
+    Wm, dW = wl.tensors["W"].to(dev), wl.tensors["dW"].to(dev)
+    for p2 in (False, True):
+        sfx = "_pow2" if p2 else ""
+        qm, qmt = fp8.param_requantize(Wm, transposed=True, pow2=p2)
+        sb = N * K / 16384 * (512 if p2 else 4)
+        rec("param_requant" + sfx, time_kernel(lambda: fp8.param_requantize(Wm, out=qm, pow2=p2), flush, reps),
+            bytes_=N * K * 5 + sb, workload="fp32 master W 12288x4096 -> FP8" + (", power-of-two scales" if p2 else ""))
+        rec("param_update_requant_with_T" + sfx,
+            time_kernel(lambda: fp8.param_requantize(Wm, dW, True, out=qm, out_t=qmt, pow2=p2), flush, reps),
+            bytes_=N * K * 14 + 2 * sb,
+            workload="W += dW (fp32) then FP8 W and W^T, 12288x4096" + (", power-of-two scales" if p2 else ""))
+    del Wm, dW, qm, qmt
+    torch.cuda.empty_cache()
+
     # backward
     wl = synth.backward()
     dY, Wb, Xb = (wl.tensors[k].to(dev) for k in ("dY", "W", "X"))
@@ -361,6 +377,13 @@ def _case_quant(kind):
             X = synth.backward().tensors["X"].to(dev)
             q = fp8.quantize_group(X, "M")
             return lambda: fp8.quantize_group(X, "M", out=q), None
+        if kind in ("param", "param_update"):
+            wl = synth.fp8_param()
+            Wm, dW = wl.tensors["W"].to(dev), wl.tensors["dW"].to(dev)
+            q, qt = fp8.param_requantize(Wm, transposed=True)
+            if kind == "param":
+                return lambda: fp8.param_requantize(Wm, out=q), None
+            return lambda: fp8.param_requantize(Wm, dW, True, out=q, out_t=qt), None
         if kind == "mx_t":
             X = synth.backward().tensors["X"].to(dev)
             q = fp8.quantize_mx(X, transposed=True)
@@ -380,7 +403,29 @@ KERNEL_CASES = {
     "quant_group_128x1_T": _case_quant("group_m"), "quant_mx_1x32": _case_quant("mx"),
     "gemm_mx_dgrad": _case_gemm("mx_dgrad"), "gemm_mx_wgrad": _case_gemm("mx_wgrad"),
     "quant_mx_32x1_T": _case_quant("mx_t"),
+    "param_requant": _case_quant("param"), "param_update_requant_with_T": _case_quant("param_update"),
 }
+
+
+def run_fp8_param_drift(args, dev):
+    """Figure 12 of the SkyRL page on synthetic weights: the cumulative FP8
+    displacement over many lr = 1e-6 sign updates, and the single-step
+    cosine against the update size, for fp32 and power-of-two scales."""
+    from block_scaled_fp8_e4m3_gb300 import param_drift, synth
+    n = args.drift_size
+    w0 = synth.fp32_master((n, n), seed=80).to(dev)
+    steps = args.drift_steps
+    marks = tuple(sorted({steps // 10, steps // 2, steps}))
+    out = {"experiment": "fp8_param_drift", "config": {
+        "master": f"{n}x{n} fp32 ~N(0,0.02), seed 80", "update": "1e-6 * (+-1), fair signs, per element and step",
+        "steps": steps, "displacement": "projection <D,M>/<M,M> (also L1, L2 ratios)"}}
+    for p2 in (False, True):
+        key = "pow2" if p2 else "fp32"
+        out[f"cumulative_{key}"] = {str(t): v for t, v in param_drift.cumulative_displacement(
+            w0, steps, 1e-6, p2, seed=81, checkpoints=marks).items()}
+        out[f"single_step_{key}"] = param_drift.single_step_cosine(
+            w0, [1e-7, 3e-7, 1e-6, 3e-6, 1e-5, 1e-4, 1e-3, 1e-2], p2, seed=82)
+    print(json.dumps(out), flush=True)
 
 
 def run_single_kernel(args, fp8, synth, dev):
@@ -457,6 +502,10 @@ def main():
     ap.add_argument("--kernel-reps", type=int, default=20)
     ap.add_argument("--kernel", default=None, choices=sorted(KERNEL_CASES),
                     help="run only this kernel on its workload (for profilers); prints its timing")
+    ap.add_argument("--experiment", default=None, choices=["fp8_param_drift"],
+                    help="run a measurement from the pages instead of the benchmark; prints one JSON line")
+    ap.add_argument("--drift-size", type=int, default=4096)
+    ap.add_argument("--drift-steps", type=int, default=2000)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -477,6 +526,9 @@ def main():
     dev = torch.device("cuda", local)
     if args.kernel is not None:
         run_single_kernel(args, fp8, synth, dev)
+        return
+    if args.experiment == "fp8_param_drift":
+        run_fp8_param_drift(args, dev)
         return
     if world > 1:
         import torch.distributed as dist

@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "FP8Error", "QTensor", "SyncEntry", "library", "quantize_group", "quantize_block", "quantize_mx",
-    "permute_rows_mx", "gemm", "grouped_gemm", "sync_payload_size", "sync_pack", "sync_install", "sync_install_noalloc",
+    "param_requantize", "permute_rows_mx", "gemm", "grouped_gemm", "sync_payload_size", "sync_pack", "sync_install", "sync_install_noalloc",
     "status_poll", "mx_scale_bytes", "mx_grouped_scale_bytes",
     "RECIPE_BLOCKWISE", "RECIPE_MX", "RECIPE_BLOCKWISE_POW2", "LAYOUT_GROUP_1x128", "LAYOUT_BLOCK_128x128", "LAYOUT_MX_1x32",
     "LAYOUT_MX_1x32_GROUPED",
@@ -74,6 +74,7 @@ def library() -> C.CDLL:
         "fp8_quantize_block": [P, I64, I64, I64, TP, TP, S],
         "fp8_quantize_mx": [P, I64, I64, I64, TP, S],
         "fp8_quantize_mx_transposed": [P, I64, I64, I64, TP, S],
+        "fp8_param_requantize": [P, P, I64, I64, I64, TP, TP, S],
         "fp8_permute_rows_mx": [TP, P, P, I32, TP, S],
         "fp8_gemm_blockscaled": [TP, TP, P, I64, I32, I32, TP, S],
         "fp8_grouped_gemm": [TP, TP, P, I32, I64, P, I64, S],
@@ -197,6 +198,37 @@ def quantize_block(w: torch.Tensor, transposed: bool = False, out: Optional[QTen
     tt = qt.c() if qt is not None else None
     _check(library().fp8_quantize_block(w.data_ptr(), N, K, w.stride(0), C.byref(t),
                                         C.byref(tt) if tt is not None else None, _stream(stream)))
+    return (q, qt) if transposed else q
+
+
+def param_requantize(master: torch.Tensor, delta: Optional[torch.Tensor] = None, transposed: bool = False,
+                     out: Optional[QTensor] = None, out_t: Optional[QTensor] = None, stream=None,
+                     pow2: bool = False):
+    """fp8_param: Q(W) of an fp32 master [N, K] in 128x128 blocks.  With a
+    delta, master += delta (fp32, in place) first.  Returns the FP8 weight
+    (and its transposed copy when transposed=True)."""
+    if master.dtype != torch.float32 or master.dim() != 2 or master.stride(1) != 1:
+        raise TypeError("master must be a row-major 2-D float32 tensor")
+    N, K = master.shape
+    dev = _dev(master)
+    if delta is not None:
+        if delta.dtype != torch.float32 or delta.shape != master.shape or delta.stride() != master.stride():
+            raise TypeError("delta must be a float32 tensor with the master's shape and strides")
+        if delta.device != master.device:
+            raise TypeError("delta must be on the master's device")
+    recipe = RECIPE_BLOCKWISE_POW2 if pow2 else RECIPE_BLOCKWISE
+    layout = LAYOUT_MX_1x32 if pow2 else LAYOUT_BLOCK_128x128
+    q = out or QTensor(torch.empty((N, K), dtype=torch.uint8, device=dev),
+                       _scales_for(N, K, pow2, (N // 128, K // 128), dev), N, K, recipe, layout)
+    qt = None
+    if transposed:
+        qt = out_t or QTensor(torch.empty((K, N), dtype=torch.uint8, device=dev),
+                              _scales_for(K, N, pow2, (K // 128, N // 128), dev), K, N, recipe, layout)
+    t = q.c()
+    tt = qt.c() if qt is not None else None
+    _check(library().fp8_param_requantize(master.data_ptr(), delta.data_ptr() if delta is not None else None, N, K,
+                                          master.stride(0), C.byref(t), C.byref(tt) if tt is not None else None,
+                                          _stream(stream)))
     return (q, qt) if transposed else q
 
 

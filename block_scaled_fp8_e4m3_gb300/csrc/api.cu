@@ -387,6 +387,33 @@ fp8_status fp8_quantize_block(const void* w_bf16, int64_t N, int64_t K, int64_t 
     return e == cudaSuccess ? FP8_OK : cuda_fail(e, "quantize_block");
 }
 
+fp8_status fp8_param_requantize(float* master, const float* delta, int64_t N, int64_t K, int64_t ld,
+                                const fp8_tensor* out, const fp8_tensor* out_t, fp8_stream_t stream) {
+    if (N < 0 || K < 0) return fail(FP8_ERR_INVALID_ARG, "master: negative size");
+    if (N > 0 && K > 0 && master == nullptr) return fail(FP8_ERR_INVALID_ARG, "master is NULL");
+    if (ld < K) return fail(FP8_ERR_INVALID_ARG, "master: ld %lld < cols %lld", (long long)ld, (long long)K);
+    if (!aligned16(master) || !aligned16(delta) || (ld % 4) != 0)
+        return fail(FP8_ERR_ALIGNMENT, "master/delta: not 16-byte aligned or ld %% 4 != 0");
+    if (N > (int64_t)INT32_MAX || K > (int64_t)INT32_MAX)
+        return fail(FP8_ERR_UNSUPPORTED, "master: dimension above 2^31-1");
+    if (N % 128 != 0 || K % 128 != 0)
+        return fail(FP8_ERR_UNSUPPORTED, "128x128 blocks need N, K multiples of 128 (N = %lld, K = %lld)", (long long)N,
+                    (long long)K);
+    const bool pow2 = out != nullptr && out->recipe == FP8_RECIPE_BLOCKWISE_POW2;
+    const int recipe = pow2 ? FP8_RECIPE_BLOCKWISE_POW2 : FP8_RECIPE_BLOCKWISE_FP32;
+    const int layout = pow2 ? FP8_LAYOUT_MX_1x32 : FP8_LAYOUT_BLOCK_128x128;
+    fp8_status s = check_out(out, "out", recipe, layout, N, K);
+    if (s != FP8_OK) return s;
+    if (out_t != nullptr) {
+        s = check_out(out_t, "out_t", recipe, layout, K, N);
+        if (s != FP8_OK) return s;
+    }
+    cudaError_t e = launch_param_requant(master, delta, N, K, ld, static_cast<uint8_t*>(out->codes), out->scales,
+                                         out_t ? static_cast<uint8_t*>(out_t->codes) : nullptr,
+                                         out_t ? out_t->scales : nullptr, pow2, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : cuda_fail(e, "param_requantize");
+}
+
 fp8_status fp8_quantize_mx(const void* x_bf16, int64_t R, int64_t K, int64_t ld, const fp8_tensor* out,
                            fp8_stream_t stream) {
     fp8_status s = check_input(x_bf16, R, K, ld, "x");

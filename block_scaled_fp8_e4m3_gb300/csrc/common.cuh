@@ -61,9 +61,12 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
     return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
-// Blockwise scale s = amax / 448 (IEEE fp32 quotient); 1 for an all-zero group.
+// Blockwise scale s = amax / 448 (IEEE fp32 quotient); 1 for an all-zero
+// group and whenever the quotient underflows to 0 (amax below 448 * 2^-150,
+// possible only for fp32 inputs), so no block divides by zero.
 __device__ __forceinline__ float group_scale(float amax) {
-    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+    const float s = __fdiv_rn(amax, 448.0f);
+    return s == 0.0f ? 1.0f : s;
 }
 
 // The same scale for a group maximum that is a bf16 value: Markstein's FMA
@@ -138,11 +141,11 @@ __device__ __forceinline__ float exp2_int(int k) {
 
 // Exponent of the blockwise recipe's power-of-two scale: e = ceil(log2(t)),
 // t = RN(amax/448) the fp32 recipe's scale, i.e. the smallest power of two
-// not below t; clamped to the E8M0 range [-127, 127]; 0 (s = 1) for an
-// all-zero group.  amax is a bf16 value or +inf.
-__device__ __forceinline__ int pow2_exponent(float amax) {
-    if (amax == 0.0f) return 0;
-    const uint32_t u = __float_as_uint(group_scale_bf16(amax));
+// not below t; clamped to the E8M0 range [-127, 127].  pow2_exponent takes
+// the group maximum amax (a bf16 value or +inf) and gives 0 (s = 1) for an
+// all-zero group.
+__device__ __forceinline__ int pow2_exponent_of_scale(float t) {
+    const uint32_t u = __float_as_uint(t);
     const int bexp = (int)(u >> 23);
     const uint32_t m = u & 0x7FFFFFu;
     int e;
@@ -151,8 +154,12 @@ __device__ __forceinline__ int pow2_exponent(float amax) {
     else if (bexp != 0)
         e = bexp - 127 + (m != 0u ? 1 : 0);
     else
-        e = (31 - __clz(m)) - 149 + ((m & (m - 1u)) != 0u ? 1 : 0);
+        e = (31 - __clz(m)) - 149 + ((m & (m - 1u)) != 0u ? 1 : 0);  // t = 0 gives -150
     return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+__device__ __forceinline__ int pow2_exponent(float amax) {
+    return amax == 0.0f ? 0 : pow2_exponent_of_scale(group_scale_bf16(amax));
 }
 
 // Byte offset of the E8M0 scale of (row r, 32-column block j) in the

@@ -21,6 +21,9 @@ cudaError_t launch_quant_block(const uint16_t* w, int64_t N, int64_t K, int64_t 
                                void* scales, uint8_t* codes_t, void* scales_t, bool pow2, cudaStream_t st);
 cudaError_t launch_quant_mx(const uint16_t* x, int64_t R, int64_t K, int64_t ld, uint8_t* codes, uint8_t* scales,
                             cudaStream_t st);
+cudaError_t launch_param_requant(float* master, const float* delta, int64_t N, int64_t K, int64_t ld,
+                                 uint8_t* codes, void* scales, uint8_t* codes_t, void* scales_t, bool pow2,
+                                 cudaStream_t st);
 cudaError_t launch_quant_mx_t(const uint16_t* x, int64_t R, int64_t K, int64_t ld, uint8_t* codes_t,
                               uint8_t* scales_t, cudaStream_t st);
 cudaError_t launch_permute_rows_mx(const uint8_t* src_codes, const uint8_t* src_scales, int64_t src_rows,

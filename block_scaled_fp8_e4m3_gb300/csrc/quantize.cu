@@ -254,6 +254,29 @@ __global__ void __launch_bounds__(256) k_quant_group_m(const uint16_t* __restric
     }
 }
 
+// Writes a 128x128 code tile held in shared memory (row stride kStride)
+// transposed: thread t (of 256) takes column t%128 and 64 of its rows, and
+// writes them as 64 contiguous bytes of row t%128 of dst (leading dim ld).
+template <int kStride>
+__device__ __forceinline__ void store_tile_transposed(const uint8_t* tile, int t, uint8_t* dst, int64_t ld) {
+    const int col = t & 127, half = t >> 7;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+        const int r0 = half * 64 + part * 32;
+        uint32_t wds[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            uint32_t wd = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) wd |= (uint32_t)tile[(r0 + q * 4 + b) * kStride + col] << (8 * b);
+            wds[q] = wd;
+        }
+        uint4* d = reinterpret_cast<uint4*>(dst + col * ld + r0);
+        d[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+        d[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // 128x128 blocks.  Block = one weight block; thread (chunk = t%16, rg = t/16)
 // holds rows 8rg..8rg+7 of columns 8chunk..8chunk+7 (eight 16-byte loads in
@@ -324,22 +347,106 @@ __global__ void __launch_bounds__(256) k_quant_block(const uint16_t* __restrict_
     }
     if (codes_t == nullptr) return;
     __syncthreads();
-    const int col = t & 127, half = t >> 7;
+    store_tile_transposed<kStride>(tile, t, codes_t + k0 * N + n0, N);
+}
+
+// ---------------------------------------------------------------------------
+// fp8_param: the FP8 storage of a weight recomputed from its fp32 master
+// ("Deep dive: FP8 quantization with FP32 and power-of-two block scales": the
+// optimizer updates the FP32 master, and after every step it is quantized
+// again into the FP8 parameters).  Block = one 128x128 block of the master;
+// thread (lane, warp) holds rows 16warp..16warp+15 of columns
+// 4lane..4lane+3 (sixteen 16-byte loads; each row is one 512-byte warp
+// access).  With kDelta the step's final add W += dW (fp32, round to
+// nearest) is applied first and written back.  fp32 recipe: s = RN(amax/448),
+// 1 when that is 0; codes from the IEEE quotient w/s (fp32 inputs have full
+// 24-bit significands, so the division is the IEEE one).  Power-of-two
+// recipe: e from RN(amax/448), codes from the exact product w * 2^-e.
+// ---------------------------------------------------------------------------
+template <bool kPow2, bool kDelta>
+__global__ void __launch_bounds__(256) k_param_requant(float* __restrict__ master, const float* __restrict__ delta,
+                                                       int64_t N, int64_t K, int64_t ld, uint8_t* __restrict__ codes,
+                                                       void* __restrict__ scales, uint8_t* __restrict__ codes_t,
+                                                       void* __restrict__ scales_t) {
+    constexpr int kStride = 144;
+    __shared__ float red[8];
+    __shared__ __align__(16) uint8_t tile[128 * kStride];
+
+    const int64_t KB = K / 128, NB = N / 128;
+    const int64_t nb = (int64_t)blockIdx.x / KB, kb = (int64_t)blockIdx.x % KB;
+    const int64_t n0 = nb * 128, k0 = kb * 128;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    float* base = master + (n0 + warp * 16) * ld + k0 + lane * 4;
+
+    float4 v[16];
+    if (kDelta) {
+        const float* dbase = delta + (n0 + warp * 16) * ld + k0 + lane * 4;
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-        const int r0 = half * 64 + part * 32;
-        uint32_t wds[8];
+        for (int h = 0; h < 2; ++h) {
+            float4 d[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            uint32_t wd = 0;
+            for (int i = 0; i < 8; ++i) {
+                v[8 * h + i] = __ldcs(reinterpret_cast<const float4*>(base + (8 * h + i) * ld));
+                d[i] = __ldcs(reinterpret_cast<const float4*>(dbase + (8 * h + i) * ld));
+            }
 #pragma unroll
-            for (int b = 0; b < 4; ++b) wd |= (uint32_t)tile[(r0 + q * 4 + b) * kStride + col] << (8 * b);
-            wds[q] = wd;
+            for (int i = 0; i < 8; ++i) {
+                float4& w = v[8 * h + i];
+                w.x = __fadd_rn(w.x, d[i].x);
+                w.y = __fadd_rn(w.y, d[i].y);
+                w.z = __fadd_rn(w.z, d[i].z);
+                w.w = __fadd_rn(w.w, d[i].w);
+                __stcs(reinterpret_cast<float4*>(base + (8 * h + i) * ld), w);
+            }
         }
-        uint4* dst = reinterpret_cast<uint4*>(codes_t + (k0 + col) * N + n0 + r0);
-        dst[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
-        dst[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __ldcs(reinterpret_cast<const float4*>(base + i * ld));
     }
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a = fmaxf(fmaxf(a, fmaxf(fabsf(v[i].x), fabsf(v[i].y))),
+                                           fmaxf(fabsf(v[i].z), fabsf(v[i].w)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (lane == 0) red[warp] = a;
+    __syncthreads();
+    a = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) a = fmaxf(a, red[i]);
+    float s = 1.0f, mul = 1.0f;
+    if (kPow2) {
+        const int e = a == 0.0f ? 0 : pow2_exponent_of_scale(__fdiv_rn(a, 448.0f));
+        mul = exp2_int(-e);
+        const uint32_t b4 = (uint32_t)(e + 127) * 0x01010101u;
+        const uint4 fill = make_uint4(b4, b4, b4, b4);
+        if (t < 32) reinterpret_cast<uint4*>(static_cast<uint8_t*>(scales) + (nb * KB + kb) * 512)[t] = fill;
+        else if (t < 64 && scales_t)
+            reinterpret_cast<uint4*>(static_cast<uint8_t*>(scales_t) + (kb * NB + nb) * 512)[t - 32] = fill;
+    } else {
+        s = group_scale(a);
+        if (t == 0) {
+            static_cast<float*>(scales)[nb * KB + kb] = s;
+            if (scales_t) static_cast<float*>(scales_t)[kb * NB + nb] = s;
+        }
+    }
+    uint8_t* crow = codes + (n0 + warp * 16) * K + k0 + lane * 4;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float q0, q1, q2, q3;
+        if (kPow2) {
+            q0 = v[i].x * mul; q1 = v[i].y * mul; q2 = v[i].z * mul; q3 = v[i].w * mul;
+        } else {
+            q0 = __fdiv_rn(v[i].x, s); q1 = __fdiv_rn(v[i].y, s);
+            q2 = __fdiv_rn(v[i].z, s); q3 = __fdiv_rn(v[i].w, s);
+        }
+        const uint32_t c = e4m3x2(q0, q1) | (e4m3x2(q2, q3) << 16);
+        *reinterpret_cast<uint32_t*>(crow + i * K) = c;
+        if (codes_t) *reinterpret_cast<uint32_t*>(tile + (warp * 16 + i) * kStride + lane * 4) = c;
+    }
+    if (codes_t == nullptr) return;
+    __syncthreads();
+    store_tile_transposed<kStride>(tile, t, codes_t + k0 * N + n0, N);
 }
 
 // ---------------------------------------------------------------------------
@@ -562,6 +669,25 @@ cudaError_t launch_quant_block(const uint16_t* w, int64_t N, int64_t K, int64_t 
         k_quant_block<true><<<(unsigned)blocks, 256, 0, st>>>(w, N, K, ld, codes, scales, codes_t, scales_t);
     else
         k_quant_block<false><<<(unsigned)blocks, 256, 0, st>>>(w, N, K, ld, codes, scales, codes_t, scales_t);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_param_requant(float* master, const float* delta, int64_t N, int64_t K, int64_t ld,
+                                 uint8_t* codes, void* scales, uint8_t* codes_t, void* scales_t, bool pow2,
+                                 cudaStream_t st) {
+    if (N == 0 || K == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((N / 128) * (K / 128));
+    if (pow2) {
+        if (delta)
+            k_param_requant<true, true><<<blocks, 256, 0, st>>>(master, delta, N, K, ld, codes, scales, codes_t, scales_t);
+        else
+            k_param_requant<true, false><<<blocks, 256, 0, st>>>(master, delta, N, K, ld, codes, scales, codes_t, scales_t);
+    } else {
+        if (delta)
+            k_param_requant<false, true><<<blocks, 256, 0, st>>>(master, delta, N, K, ld, codes, scales, codes_t, scales_t);
+        else
+            k_param_requant<false, false><<<blocks, 256, 0, st>>>(master, delta, N, K, ld, codes, scales, codes_t, scales_t);
+    }
     return cudaGetLastError();
 }
 

@@ -16,6 +16,11 @@ Workloads (matrices follow torch ``nn.Linear``: X [M,K], W [N,K], Y = X W^T):
 * ``moe``       seed 4: top-8 routing of 16384 tokens over 64 experts with
                 Zipf(1.1) expert popularity, then X [16384,2048] ~N(0,1),
                 W [64,1024,2048] ~N(0,0.02)
+* ``fp8_param`` seed 5: fp32 master W [12288,4096] ~N(0,0.02) (kept in
+                fp32), then one optimizer update dW = 1e-6 * (+-1) with
+                independent fair signs: an Adam-like step whose magnitude is
+                the learning rate (the pages report max |dW| = 1.01e-6 and a
+                mean relative update of 0.6-0.9e-4; 1e-6 / E|W| = 0.63e-4)
 
 "Outliers": exactly round(0.001 * numel) distinct positions, drawn uniformly
 without replacement (``randperm``), are multiplied by 50 before the bf16
@@ -130,6 +135,27 @@ def moe(tokens: int = 16384, experts: int = 64, top_k: int = 8, hidden: int = 20
                     f"{ffn}x{hidden}", seed,
                     {"X": X, "W": W, "gather": gather, "offsets": offsets},
                     {"tokens": tokens, "experts": experts, "top_k": top_k})
+
+
+def fp32_master(shape, seed: int, std: float = 0.02) -> torch.Tensor:
+    """fp32 master weights ~N(0, std), not rounded to bf16."""
+    x = torch.randn(*shape, generator=_gen(seed), dtype=torch.float32)
+    return x.mul_(std)
+
+
+def sign_updates(shape, seed: int, lr: float = 1e-6, gen: torch.Generator = None, device=None) -> torch.Tensor:
+    """lr * (+-1) with independent fair signs, fp32 (on `device` with `gen`
+    when given, for long update sequences drawn where they are used)."""
+    g = gen if gen is not None else _gen(seed)
+    b = torch.randint(0, 2, tuple(shape), generator=g, dtype=torch.int32, device=device)
+    return (b.to(torch.float32) * 2.0 - 1.0).mul_(lr)
+
+
+def fp8_param(N: int = 12288, K: int = 4096, seed: int = 5, lr: float = 1e-6) -> Workload:
+    g = _gen(seed)
+    W = torch.randn(N, K, generator=g, dtype=torch.float32).mul_(0.02)
+    dW = sign_updates((N, K), seed, lr, gen=g)
+    return Workload(f"fp8_param {N}x{K}", seed, {"W": W, "dW": dW}, {"lr": lr})
 
 
 def random_bf16(shape, seed: int, std: float = 1.0, outliers: bool = False) -> torch.Tensor:

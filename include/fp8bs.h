@@ -167,6 +167,27 @@ fp8_status fp8_quantize_block(const void* w_bf16, int64_t N, int64_t K, int64_t 
                               const fp8_tensor* out, const fp8_tensor* out_t,
                               fp8_stream_t stream);
 
+/* fp8_param: recomputes the FP8 storage of a weight from its fp32 master,
+ * optionally applying the optimizer step's final add first.  [SkyRL]
+ * overview: FP8 parameters plus an FP32 master weight, with no BF16 copy;
+ * "Deep dive: FP8 quantization with FP32 and power-of-two block scales":
+ * the optimizer updates the FP32 master and re-quantizes it into the FP8
+ * storage after every step, Q(W_t) from the current master.
+ *  master: fp32 [N][ld] on the device (first K columns used), 16-byte
+ *          aligned, ld % 4 == 0.  Written only when delta is non-NULL.
+ *  delta:  NULL, or fp32 [N][ld] (same ld): master <- RN(master + delta)
+ *          element by element before quantizing (the update is not kept).
+ *  out:    codes [N][K] and 128x128 block scales of the (updated) master;
+ *          FP8_RECIPE_BLOCKWISE_FP32 with FP8_LAYOUT_BLOCK_128x128 (fp32
+ *          scales s = RN(amax/448), 1 for a block whose quotient is 0, codes
+ *          from the IEEE quotient w/s), or FP8_RECIPE_BLOCKWISE_POW2 with
+ *          FP8_LAYOUT_MX_1x32 (E8M0 exponents, codes from w * 2^-e).
+ *  out_t:  NULL or the transposed copy [K][N] in the same recipe.
+ * Requires N % 128 == 0, K % 128 == 0.  Errors: INVALID_ARG / ALIGNMENT /
+ * UNSUPPORTED before anything is enqueued; the call is asynchronous. */
+fp8_status fp8_param_requantize(float* master, const float* delta, int64_t N, int64_t K, int64_t ld,
+                                const fp8_tensor* out, const fp8_tensor* out_t, fp8_stream_t stream);
+
 /* MXFP8 quantization of x [R][ld] (first K columns) in 1x32 blocks with E8M0
  * scales.  [SkyRL] "独立した量子化がポリシーの一貫性を崩す場合": one scale per
  * 1x32 block in the MXFP8 recipe; "Deep dive: FP8 quantization with FP32

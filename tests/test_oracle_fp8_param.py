@@ -122,3 +122,20 @@ def test_scale_corner_cases(orc):
     assert e_tiny == 0                                                 # 2^-127 (clamped)
     assert np.all(c2[:, 128:256] == 0)
     assert s2[orc.mx_scale_offset(0, 0, 512)] == 127                  # all-zero: e = 0
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_displacement_projection_is_near_one(orc, pow2):
+    """[SkyRL] Figure 12, left, on the oracle: after many lr = 1e-6 sign
+    updates the FP8 displacement projected on the master's equals the
+    master's displacement on average (no update is systematically lost)."""
+    w0 = _master((256, 256), 11)
+    rng = np.random.default_rng(12)
+    deq = (lambda c, s: orc.dequant_mx(c, s)) if pow2 else (lambda c, s: orc.dequant_block(c, s))
+    d0 = deq(*orc.quant_block_128x128_f32(w0, pow2=pow2))
+    w = w0
+    for _ in range(300):
+        w = orc.param_update(w, rng.choice(np.array([-1e-6, 1e-6], np.float32), w.shape))
+    D = deq(*orc.quant_block_128x128_f32(w, pow2=pow2)) - d0
+    M = w.astype(np.float64) - w0
+    assert 0.85 < float((D * M).sum() / (M * M).sum()) < 1.15
