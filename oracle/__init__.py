@@ -49,6 +49,9 @@ def load():
         "oracle_param_update": (None, [_P, _P, _I64, _I64, _I64]),
         "oracle_quant_block_128x128_f32": (None, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
         "oracle_quant_block_128x128_f32_pow2": (None, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
+        "oracle_bf16_round_f64": (C.c_uint16, [C.c_double]),
+        "oracle_rmsnorm": (None, [_P, _P, _I64, _I64, _I64, C.c_float, _P, _P]),
+        "oracle_swiglu": (None, [_P, _I64, _I64, _I64, _P]),
         "oracle_dequant_group": (None, [_P, _P, _I64, _I64, _P]),
         "oracle_dequant_block": (None, [_P, _P, _I64, _I64, _P]),
         "oracle_dequant_mx": (None, [_P, _P, _I64, _I64, _P]),
@@ -237,6 +240,36 @@ def quant_block_128x128_f32(w, transposed: bool = False, pow2: bool = False):
     if transposed:
         return codes, scales, codes_t, scales_t
     return codes, scales
+
+
+# ---------------------------------------------------------------- fused producers
+def bf16_round(values) -> np.ndarray:
+    """bf16 bit patterns nearest to each (fp64) value."""
+    v = np.asarray(values, np.float64)
+    fn = load().oracle_bf16_round_f64
+    return np.array([fn(float(a)) for a in v.ravel()], np.uint16).reshape(v.shape)
+
+
+def rmsnorm(x_bits, gamma_bits, eps: float):
+    """RMSNorm in fp64, output rounded to bf16: (y bits [M, K], rstd fp32 [M])."""
+    x = _bits(x_bits)
+    g = _bits(gamma_bits)
+    M, K = x.shape
+    assert g.shape == (K,)
+    y = np.empty((M, K), np.uint16)
+    rstd = np.empty((M,), np.float32)
+    load().oracle_rmsnorm(_ptr(x), _ptr(g), M, K, K, float(eps), _ptr(y), _ptr(rstd))
+    return y, rstd
+
+
+def swiglu(gu_bits):
+    """silu(gate) * up of a [M, 2F] row pair in fp64, rounded to bf16: [M, F]."""
+    gu = _bits(gu_bits)
+    M, F2 = gu.shape
+    F = F2 // 2
+    h = np.empty((M, F), np.uint16)
+    load().oracle_swiglu(_ptr(gu), M, F, F2, _ptr(h))
+    return h
 
 
 # ---------------------------------------------------------------- dequant

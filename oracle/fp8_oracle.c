@@ -584,6 +584,85 @@ void oracle_quant_block_128x128_f32_pow2(const float* w, int64_t N, int64_t K, i
 }
 
 /* ------------------------------------------------------------------------ */
+/* Producers fused with the quantization ([P3] "Kwantisatieschema": the      */
+/* activations saved for the backward pass are stored in FP8, fused with the */
+/* previous operator; "Implementatie": fused activation / RMSNorm kernels).  */
+/* The oracle computes each producer in fp64 and rounds its output once to   */
+/* bf16; the quantizers above then take that bf16 tensor, so the fused      */
+/* operation equals the producer followed by the quantizer.                  */
+/* ------------------------------------------------------------------------ */
+
+/* bf16 nearest to an exact real value (round to nearest, ties to even;
+ * overflow to +-inf; bf16 subnormals down to 2^-133; NaN -> 0x7FC0|sign).
+ * Works on the double's binary exponent like oracle_e4m3_encode_f64. */
+uint16_t oracle_bf16_round_f64(double v)
+{
+    uint16_t sign = (uint16_t)((f64_bits(v) >> 63) << 15);
+    if (isnan(v))
+        return sign | 0x7FC0;
+    double a = fabs(v);
+    if (isinf(a))
+        return sign | 0x7F80;
+    if (a == 0.0 || a < ldexp(1.0, -140))   /* far below half the smallest step */
+        return sign;
+    int ex = ilogb(a);                       /* floor(log2 a) */
+    int qe = (ex >= -126 ? ex : -126) - 7;   /* exponent of the grid spacing */
+    double t = ldexp(a, -qe);                /* exact: a / 2^qe */
+    double fl = floor(t);
+    double rem = t - fl;                     /* exact */
+    uint64_t q = (uint64_t)fl;
+    if (rem > 0.5 || (rem == 0.5 && (q & 1)))
+        q += 1;
+    if (ex < -126)                           /* subnormal grid: q steps of 2^-133 */
+        return sign | (uint16_t)q;           /* q = 128 is 2^-126, bits 0x0080 */
+    if (q == 256) {
+        q = 128;
+        ex += 1;
+    }
+    int E = ex + 127;
+    if (E >= 255)
+        return sign | 0x7F80;
+    return sign | (uint16_t)((E << 7) | (int)(q - 128));
+}
+
+/* RMSNorm: y[r][k] = x[r][k] * rstd[r] * gamma[k] with rstd = 1 / sqrt(mean_k
+ * x[r][k]^2 + eps), all in fp64, y rounded once to bf16; rstd returned as
+ * fp32 (saved for the backward pass).  x bf16 [M][ld], gamma bf16 [K],
+ * y bf16 [M][K]. */
+void oracle_rmsnorm(const uint16_t* x, const uint16_t* gamma, int64_t M, int64_t K, int64_t ld, float eps,
+                    uint16_t* y, float* rstd)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < M; ++r) {
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double v = (double)bf16_bits_to_f32(x[r * ld + k]);
+            ss += v * v;
+        }
+        double rs = 1.0 / sqrt(ss / (double)K + (double)eps);
+        if (rstd) rstd[r] = (float)rs;
+        for (int64_t k = 0; k < K; ++k)
+            y[r * K + k] = oracle_bf16_round_f64((double)bf16_bits_to_f32(x[r * ld + k]) * rs *
+                                                 (double)bf16_bits_to_f32(gamma[k]));
+    }
+}
+
+/* SwiGLU: h[r][f] = silu(g) * u with g = gu[r][f], u = gu[r][F + f] (the
+ * gate and up projections side by side in one [M][2F] row), silu(g) =
+ * g / (1 + exp(-g)), in fp64, h rounded once to bf16.  gu bf16 [M][ld],
+ * ld >= 2F; h bf16 [M][F]. */
+void oracle_swiglu(const uint16_t* gu, int64_t M, int64_t F, int64_t ld, uint16_t* h)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < M; ++r)
+        for (int64_t f = 0; f < F; ++f) {
+            double g = (double)bf16_bits_to_f32(gu[r * ld + f]);
+            double u = (double)bf16_bits_to_f32(gu[r * ld + F + f]);
+            h[r * F + f] = oracle_bf16_round_f64(g / (1.0 + exp(-g)) * u);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Dequantization (exact in fp64: a 4-bit significand times a 24-bit scale).  */
 /* ------------------------------------------------------------------------ */
 

@@ -52,6 +52,7 @@ def _t(rows, cols, recipe, layout, codes=0x10000, scales=0x20000):
     ("misaligned", 2), ("bad_ld", 1), ("wrong_layout", 1), ("wrong_shape", 1), ("null_out", 1),
     ("gemm_bad_K", 3), ("gemm_K_mismatch", 1), ("gemm_bad_N", 3),
     ("mx_t_bad_R", 3), ("mx_t_wrong_shape", 1),
+    ("param_bad_N", 3), ("param_bad_ld", 2), ("param_wrong_recipe", 1),
 ])
 def test_argument_validation_happens_on_host(lib, case, expect):
     x = 0x100000                                   # never dereferenced: validation fails first
@@ -74,6 +75,15 @@ def test_argument_validation_happens_on_host(lib, case, expect):
     elif case == "mx_t_wrong_shape":
         t = _t(128, 64, 2, 3)                      # must be (K, R) = (64, 128)
         st = lib.fp8_quantize_mx_transposed(x, 128, 64, 64, C.byref(t), s)
+    elif case == "param_bad_N":
+        t = _t(100, 128, 1, 2)
+        st = lib.fp8_param_requantize(x, None, 100, 128, 128, C.byref(t), None, s)
+    elif case == "param_bad_ld":
+        t = _t(128, 128, 1, 2)
+        st = lib.fp8_param_requantize(x, None, 128, 128, 130, C.byref(t), None, s)
+    elif case == "param_wrong_recipe":
+        t = _t(128, 128, 2, 3)                     # MXFP8 is not an fp8_param recipe
+        st = lib.fp8_param_requantize(x, x, 128, 128, 128, C.byref(t), None, s)
     elif case == "misaligned":
         t = _t(4, 128, 1, 1)
         st = lib.fp8_quantize_group(x + 2, 4, 128, 128, 0, C.byref(t), s)
