@@ -258,6 +258,24 @@ def breakdown(fp8, synth, dev, flush, pk, reps):
     del Wm, dW, qm, qmt
     torch.cuda.empty_cache()
 
+    # producers fused with the activation quantization
+    X = synth.mlp().tensors["X"].to(dev)
+    gam = torch.ones((K,), dtype=torch.bfloat16, device=dev)
+    for rc, nm in ((fp8.RECIPE_BLOCKWISE, ""), (fp8.RECIPE_MX, "_mx")):
+        qn = fp8.rmsnorm_quantize(X, gam, 1e-6, rc)
+        sbytes = 4 / 128 if rc == fp8.RECIPE_BLOCKWISE else 1 / 32
+        rec("rmsnorm_quant" + nm, time_kernel(lambda: fp8.rmsnorm_quantize(X, gam, 1e-6, rc, out=qn), flush, reps),
+            bytes_=M * K * (3 + sbytes), workload="RMSNorm of X 8192x4096 -> FP8" + (" MX" if nm else " 1x128"))
+    GU = torch.empty((M, N), dtype=torch.bfloat16, device=dev).normal_(0.0, 1.5)
+    for rc, nm in ((fp8.RECIPE_BLOCKWISE, ""), (fp8.RECIPE_MX, "_mx")):
+        qs = fp8.swiglu_quantize(GU, rc)
+        sbytes = 4 / 128 if rc == fp8.RECIPE_BLOCKWISE else 1 / 32
+        rec("swiglu_quant" + nm, time_kernel(lambda: fp8.swiglu_quantize(GU, rc, out=qs), flush, reps),
+            bytes_=M * (N // 2) * (5 + sbytes),
+            workload="SwiGLU of the 8192x12288 up projection -> FP8 8192x6144" + (" MX" if nm else " 1x128"))
+    del X, gam, qn, GU, qs
+    torch.cuda.empty_cache()
+
     # backward
     wl = synth.backward()
     dY, Wb, Xb = (wl.tensors[k].to(dev) for k in ("dY", "W", "X"))
@@ -377,6 +395,15 @@ def _case_quant(kind):
             X = synth.backward().tensors["X"].to(dev)
             q = fp8.quantize_group(X, "M")
             return lambda: fp8.quantize_group(X, "M", out=q), None
+        if kind in ("rmsnorm", "swiglu"):
+            if kind == "rmsnorm":
+                X = synth.mlp().tensors["X"].to(dev)
+                gam = torch.ones((X.shape[1],), dtype=torch.bfloat16, device=dev)
+                q = fp8.rmsnorm_quantize(X, gam)
+                return lambda: fp8.rmsnorm_quantize(X, gam, out=q), None
+            GU = torch.empty((M, N), dtype=torch.bfloat16, device=dev).normal_(0.0, 1.5)
+            q = fp8.swiglu_quantize(GU)
+            return lambda: fp8.swiglu_quantize(GU, out=q), None
         if kind in ("param", "param_update"):
             wl = synth.fp8_param()
             Wm, dW = wl.tensors["W"].to(dev), wl.tensors["dW"].to(dev)
@@ -404,6 +431,7 @@ KERNEL_CASES = {
     "gemm_mx_dgrad": _case_gemm("mx_dgrad"), "gemm_mx_wgrad": _case_gemm("mx_wgrad"),
     "quant_mx_32x1_T": _case_quant("mx_t"),
     "param_requant": _case_quant("param"), "param_update_requant_with_T": _case_quant("param_update"),
+    "rmsnorm_quant": _case_quant("rmsnorm"), "swiglu_quant": _case_quant("swiglu"),
 }
 
 

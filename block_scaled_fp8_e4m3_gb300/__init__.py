@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "FP8Error", "QTensor", "SyncEntry", "library", "quantize_group", "quantize_block", "quantize_mx",
-    "param_requantize", "permute_rows_mx", "gemm", "grouped_gemm", "sync_payload_size", "sync_pack", "sync_install", "sync_install_noalloc",
+    "param_requantize", "rmsnorm_quantize", "swiglu_quantize", "permute_rows_mx", "gemm", "grouped_gemm", "sync_payload_size", "sync_pack", "sync_install", "sync_install_noalloc",
     "status_poll", "mx_scale_bytes", "mx_grouped_scale_bytes",
     "RECIPE_BLOCKWISE", "RECIPE_MX", "RECIPE_BLOCKWISE_POW2", "LAYOUT_GROUP_1x128", "LAYOUT_BLOCK_128x128", "LAYOUT_MX_1x32",
     "LAYOUT_MX_1x32_GROUPED",
@@ -75,6 +75,8 @@ def library() -> C.CDLL:
         "fp8_quantize_mx": [P, I64, I64, I64, TP, S],
         "fp8_quantize_mx_transposed": [P, I64, I64, I64, TP, S],
         "fp8_param_requantize": [P, P, I64, I64, I64, TP, TP, S],
+        "fp8_rmsnorm_quantize": [P, P, I64, I64, I64, C.c_float, P, I64, P, TP, S],
+        "fp8_swiglu_quantize": [P, I64, I64, I64, P, I64, TP, S],
         "fp8_permute_rows_mx": [TP, P, P, I32, TP, S],
         "fp8_gemm_blockscaled": [TP, TP, P, I64, I32, I32, TP, S],
         "fp8_grouped_gemm": [TP, TP, P, I32, I64, P, I64, S],
@@ -230,6 +232,60 @@ def param_requantize(master: torch.Tensor, delta: Optional[torch.Tensor] = None,
                                           master.stride(0), C.byref(t), C.byref(tt) if tt is not None else None,
                                           _stream(stream)))
     return (q, qt) if transposed else q
+
+
+def _activation_out(rows: int, cols: int, recipe: int, dev) -> QTensor:
+    if recipe == RECIPE_BLOCKWISE:
+        return QTensor(torch.empty((rows, cols), dtype=torch.uint8, device=dev),
+                       torch.empty((cols // 128, rows), dtype=torch.float32, device=dev), rows, cols, recipe,
+                       LAYOUT_GROUP_1x128)
+    if recipe in (RECIPE_BLOCKWISE_POW2, RECIPE_MX):
+        return QTensor(torch.empty((rows, cols), dtype=torch.uint8, device=dev),
+                       torch.empty((mx_scale_bytes(rows, cols),), dtype=torch.uint8, device=dev), rows, cols, recipe,
+                       LAYOUT_MX_1x32)
+    raise ValueError(f"unsupported activation recipe {recipe}")
+
+
+def rmsnorm_quantize(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, recipe: int = RECIPE_BLOCKWISE,
+                     want_y: bool = False, want_rstd: bool = False, out: Optional[QTensor] = None,
+                     y: Optional[torch.Tensor] = None, rstd: Optional[torch.Tensor] = None, stream=None):
+    """RMSNorm of bf16 rows fused with their quantization.  Returns the FP8
+    activation, plus y (bf16) and rstd (fp32) when asked for."""
+    x = _bf16_2d(x)
+    M, K = x.shape
+    dev = _dev(x)
+    if gamma.dtype != torch.bfloat16 or gamma.shape != (K,) or not gamma.is_contiguous():
+        raise TypeError("gamma must be a contiguous bf16 vector of length K")
+    q = out or _activation_out(M, K, recipe, dev)
+    if want_y and y is None:
+        y = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    if want_rstd and rstd is None:
+        rstd = torch.empty((M,), dtype=torch.float32, device=dev)
+    t = q.c()
+    _check(library().fp8_rmsnorm_quantize(x.data_ptr(), gamma.data_ptr(), M, K, x.stride(0), float(eps),
+                                          y.data_ptr() if y is not None else None, y.stride(0) if y is not None else 0,
+                                          rstd.data_ptr() if rstd is not None else None, C.byref(t), _stream(stream)))
+    res = (q,) + ((y,) if want_y else ()) + ((rstd,) if want_rstd else ())
+    return res if len(res) > 1 else q
+
+
+def swiglu_quantize(gu: torch.Tensor, recipe: int = RECIPE_BLOCKWISE, want_h: bool = False,
+                    out: Optional[QTensor] = None, h: Optional[torch.Tensor] = None, stream=None):
+    """silu(gate) * up of a [M, 2F] bf16 tensor (gate | up) fused with the
+    quantization of the [M, F] result.  Returns the FP8 activation (and h)."""
+    gu = _bf16_2d(gu)
+    M, F2 = gu.shape
+    if F2 % 2:
+        raise ValueError("gu must have an even number of columns (gate | up)")
+    F = F2 // 2
+    dev = _dev(gu)
+    q = out or _activation_out(M, F, recipe, dev)
+    if want_h and h is None:
+        h = torch.empty((M, F), dtype=torch.bfloat16, device=dev)
+    t = q.c()
+    _check(library().fp8_swiglu_quantize(gu.data_ptr(), M, F, gu.stride(0), h.data_ptr() if h is not None else None,
+                                         h.stride(0) if h is not None else 0, C.byref(t), _stream(stream)))
+    return (q, h) if want_h else q
 
 
 def quantize_mx(x: torch.Tensor, out: Optional[QTensor] = None, stream=None, transposed: bool = False) -> QTensor:

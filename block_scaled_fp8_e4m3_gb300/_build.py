@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfp8bs.so")
-SOURCES = ["quantize.cu", "gemm_blockwise.cu", "gemm_mx.cu", "sync.cu", "api.cu"]
+SOURCES = ["quantize.cu", "fused.cu", "gemm_blockwise.cu", "gemm_mx.cu", "sync.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -414,6 +414,72 @@ fp8_status fp8_param_requantize(float* master, const float* delta, int64_t N, in
     return e == cudaSuccess ? FP8_OK : cuda_fail(e, "param_requantize");
 }
 
+namespace {
+// The activation recipes of the fused producers: out->recipe picks the
+// layout; returns the kernel's recipe index or -1.
+int activation_recipe(const fp8_tensor* out, int* layout) {
+    if (out == nullptr) return -1;
+    switch (out->recipe) {
+        case FP8_RECIPE_BLOCKWISE_FP32: *layout = FP8_LAYOUT_GROUP_1x128; return 0;
+        case FP8_RECIPE_BLOCKWISE_POW2: *layout = FP8_LAYOUT_MX_1x32; return 1;
+        case FP8_RECIPE_MXFP8: *layout = FP8_LAYOUT_MX_1x32; return 2;
+        default: return -1;
+    }
+}
+
+fp8_status check_bf16_out(const void* y, int64_t cols, int64_t ldy, const char* name) {
+    if (y == nullptr) return FP8_OK;
+    if (ldy < cols) return fail(FP8_ERR_INVALID_ARG, "%s: ld %lld < cols %lld", name, (long long)ldy, (long long)cols);
+    if (!aligned16(y) || ldy % 8 != 0) return fail(FP8_ERR_ALIGNMENT, "%s: not 16-byte aligned or ld %% 8 != 0", name);
+    return FP8_OK;
+}
+}  // namespace
+
+fp8_status fp8_rmsnorm_quantize(const void* x_bf16, const void* gamma_bf16, int64_t M, int64_t K, int64_t ld,
+                                float eps, void* y_bf16, int64_t ldy, float* rstd, const fp8_tensor* out,
+                                fp8_stream_t stream) {
+    fp8_status s = check_input(x_bf16, M, K, ld, "x");
+    if (s != FP8_OK) return s;
+    if (K % 128 != 0 || K == 0 || K > 8192)
+        return fail(FP8_ERR_UNSUPPORTED, "rmsnorm_quantize needs K %% 128 == 0 and 0 < K <= 8192 (K = %lld)",
+                    (long long)K);
+    if (gamma_bf16 == nullptr || !aligned16(gamma_bf16)) return fail(FP8_ERR_ALIGNMENT, "gamma NULL or misaligned");
+    if (!(eps >= 0.0f) || eps > 3.402823466e38f) return fail(FP8_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    s = check_bf16_out(y_bf16, K, ldy, "y");
+    if (s != FP8_OK) return s;
+    if (reinterpret_cast<uintptr_t>(rstd) & 3u) return fail(FP8_ERR_ALIGNMENT, "rstd misaligned");
+    int layout = 0;
+    const int rec = activation_recipe(out, &layout);
+    if (rec < 0) return fail(FP8_ERR_INVALID_ARG, "out: NULL or unsupported recipe");
+    s = check_out(out, "out", out->recipe, layout, M, K);
+    if (s != FP8_OK) return s;
+    cudaError_t e = launch_rmsnorm_quant(static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(gamma_bf16),
+                                         M, K, ld, eps, static_cast<uint16_t*>(y_bf16), ldy, rstd,
+                                         static_cast<uint8_t*>(out->codes), out->scales, rec,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : cuda_fail(e, "rmsnorm_quantize");
+}
+
+fp8_status fp8_swiglu_quantize(const void* gu_bf16, int64_t M, int64_t F, int64_t ld, void* h_bf16, int64_t ldh,
+                               const fp8_tensor* out, fp8_stream_t stream) {
+    if (F < 0 || F > (int64_t)INT32_MAX / 2) return fail(FP8_ERR_INVALID_ARG, "gu: bad F");
+    fp8_status s = check_input(gu_bf16, M, 2 * F, ld, "gu");
+    if (s != FP8_OK) return s;
+    if (F % 128 != 0) return fail(FP8_ERR_UNSUPPORTED, "swiglu_quantize needs F %% 128 == 0 (F = %lld)", (long long)F);
+    s = check_bf16_out(h_bf16, F, ldh, "h");
+    if (s != FP8_OK) return s;
+    int layout = 0;
+    const int rec = activation_recipe(out, &layout);
+    if (rec < 0) return fail(FP8_ERR_INVALID_ARG, "out: NULL or unsupported recipe");
+    s = check_out(out, "out", out->recipe, layout, M, F);
+    if (s != FP8_OK) return s;
+    if (F == 0) return FP8_OK;
+    cudaError_t e = launch_swiglu_quant(static_cast<const uint16_t*>(gu_bf16), M, F, ld, static_cast<uint16_t*>(h_bf16),
+                                        ldh, static_cast<uint8_t*>(out->codes), out->scales, rec,
+                                        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : cuda_fail(e, "swiglu_quantize");
+}
+
 fp8_status fp8_quantize_mx(const void* x_bf16, int64_t R, int64_t K, int64_t ld, const fp8_tensor* out,
                            fp8_stream_t stream) {
     fp8_status s = check_input(x_bf16, R, K, ld, "x");

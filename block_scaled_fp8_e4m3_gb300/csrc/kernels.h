@@ -26,10 +26,21 @@ cudaError_t launch_param_requant(float* master, const float* delta, int64_t N, i
                                  cudaStream_t st);
 cudaError_t launch_quant_mx_t(const uint16_t* x, int64_t R, int64_t K, int64_t ld, uint8_t* codes_t,
                               uint8_t* scales_t, cudaStream_t st);
+// Padding rows of the last MX atom row (rows >= `rows`) set to zero.
+cudaError_t zero_mx_tail(void* scales, int64_t rows, int64_t cols, cudaStream_t st);
+
 cudaError_t launch_permute_rows_mx(const uint8_t* src_codes, const uint8_t* src_scales, int64_t src_rows,
                                    int64_t K, const int32_t* gather, const int32_t* offsets, int32_t G,
                                    int64_t total, uint8_t* dst_codes, uint8_t* dst_scales, int64_t dst_scale_bytes,
                                    StatusBlock* status, cudaStream_t st);
+
+// fused.cu: recipe 0 = 1x128 fp32 scales, 1 = 1x128 power-of-two scales,
+// 2 = MXFP8 1x32 (1 and 2 write E8M0 bytes in the MX layout)
+cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, int64_t M, int64_t K, int64_t ld,
+                                 float eps, uint16_t* y, int64_t ldy, float* rstd, uint8_t* codes, void* scales,
+                                 int recipe, cudaStream_t st);
+cudaError_t launch_swiglu_quant(const uint16_t* gu, int64_t M, int64_t F, int64_t ld, uint16_t* h, int64_t ldh,
+                                uint8_t* codes, void* scales, int recipe, cudaStream_t st);
 
 // gemm_blockwise.cu, gemm_mx.cu
 struct GemmBlockwiseArgs {

@@ -188,6 +188,36 @@ fp8_status fp8_quantize_block(const void* w_bf16, int64_t N, int64_t K, int64_t 
 fp8_status fp8_param_requantize(float* master, const float* delta, int64_t N, int64_t K, int64_t ld,
                                 const fp8_tensor* out, const fp8_tensor* out_t, fp8_stream_t stream);
 
+/* Producers fused with the activation quantization.  [Jet-RL]
+ * "Kwantisatieschema": the activations saved for the backward pass are
+ * stored in FP8, fused with the operator that produces them;
+ * "Implementatie": fused activation and RMSNorm kernels.  Each computes its
+ * producer in fp32, rounds it to bf16 and quantizes those bf16 values, so
+ * the codes equal fp8_quantize_group / fp8_quantize_mx applied to the bf16
+ * output.  out->recipe selects the quantization: FP8_RECIPE_BLOCKWISE_FP32
+ * (layout FP8_LAYOUT_GROUP_1x128, fp32 scales [cols/128][rows]),
+ * FP8_RECIPE_BLOCKWISE_POW2 or FP8_RECIPE_MXFP8 (layout FP8_LAYOUT_MX_1x32,
+ * fp8_mx_scale_bytes(rows, cols) bytes).
+ *
+ * RMSNorm: y = RN_bf16(RN(x * rstd) * gamma), rstd = 1/sqrt(mean_k x^2 +
+ * eps) per row (fp32: the sum of squares in fp32, then the correctly
+ * rounded reciprocal square root).
+ *  x:     bf16 [M][ld]; gamma: bf16 [K] (16-byte aligned).
+ *  y:     NULL or bf16 [M][ldy], the normalized rows.
+ *  rstd:  NULL or fp32 [M], saved for the backward pass.
+ *  out:   codes [M][K] of y.  Requires K % 128 == 0, K <= 8192. */
+fp8_status fp8_rmsnorm_quantize(const void* x_bf16, const void* gamma_bf16, int64_t M, int64_t K, int64_t ld,
+                                float eps, void* y_bf16, int64_t ldy, float* rstd, const fp8_tensor* out,
+                                fp8_stream_t stream);
+
+/* SwiGLU: h = RN_bf16(silu(g) * u), silu(g) = g / (1 + exp(-g)), with the
+ * gate projection g in columns [0, F) and the up projection u in [F, 2F) of
+ * each row of gu (bf16 [M][ld], ld >= 2F).
+ *  h:     NULL or bf16 [M][ldh].
+ *  out:   codes [M][F] of h.  Requires F % 128 == 0. */
+fp8_status fp8_swiglu_quantize(const void* gu_bf16, int64_t M, int64_t F, int64_t ld, void* h_bf16, int64_t ldh,
+                               const fp8_tensor* out, fp8_stream_t stream);
+
 /* MXFP8 quantization of x [R][ld] (first K columns) in 1x32 blocks with E8M0
  * scales.  [SkyRL] "独立した量子化がポリシーの一貫性を崩す場合": one scale per
  * 1x32 block in the MXFP8 recipe; "Deep dive: FP8 quantization with FP32
