@@ -37,6 +37,39 @@ __device__ __forceinline__ uint4 round8_bf16(float (&f)[8]) {
     return w;
 }
 
+// Packed fp32 pair arithmetic (one instruction for two lanes of a float2).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    uint64_t x, y, d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    return r;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    uint64_t x, y, d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    return r;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Quantizes the 8 values of this lane, part of the 128-element group g of
 // row r held by the 16 lanes of a half warp (sub = lane % 16 holds elements
 // 8 sub .. 8 sub + 7 of the group).  All 32 lanes of the warp must call it
@@ -82,35 +115,38 @@ __device__ __forceinline__ void quant_group16(const float (&y)[8], bool ok, int 
 }
 
 // ---------------------------------------------------------------------------
-// RMSNorm + quantization.  One warp per row, 8 rows per 256-thread block.
-// Lane l holds chunks j < kChunks: elements 256 j + 8 l .. + 7 (each chunk is
-// one 512-byte warp access); K % 128 == 0, so the last chunk is whole or its
-// upper half warp idles.  Sum of squares in fp32 (per lane, then a warp
-// reduction), rstd = RN(1/sqrt(RN(ss/K) + eps)), y = RN_bf16(RN(x rstd) gamma).
+// RMSNorm + quantization.  A row is split into segments of 1024 elements,
+// one warp each (kW warps per row, a power of two >= K/1024; 8/kW rows per
+// 256-thread block).  Lane l of a warp holds chunks j < 4 of its segment:
+// elements 1024 seg + 256 j + 8 l .. + 7 (each chunk is one 512-byte warp
+// access; K % 128 == 0, so a chunk is whole, half or empty).  The sum of
+// squares is accumulated in fp32 per lane, reduced over the warp, and the kW
+// warp partials of a row are added in segment order through shared memory
+// (every warp of the row gets the same sum); rstd = RN(1/sqrt(RN(ss/K) +
+// eps)), y = RN_bf16(RN(x rstd) gamma).
 // ---------------------------------------------------------------------------
-template <int kRec, int kChunks>
-__global__ void __launch_bounds__(256, kChunks <= 8 ? 2 : 1) k_rmsnorm_quant(const uint16_t* __restrict__ x,
-                                                       const uint16_t* __restrict__ gamma, int64_t M, int64_t K,
-                                                       int64_t ld, float eps, uint16_t* __restrict__ y,
-                                                       int64_t ldy, float* __restrict__ rstd_out,
-                                                       uint8_t* __restrict__ codes, void* __restrict__ scales) {
-    __shared__ __align__(16) uint16_t sgamma[256 * kChunks];
-    const int lane = threadIdx.x & 31;
-    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    for (int64_t k = 8 * threadIdx.x; k < K; k += 8 * 256)
-        *reinterpret_cast<uint4*>(sgamma + k) = *reinterpret_cast<const uint4*>(gamma + k);
-    __syncthreads();
-    if (r >= M) return;
+constexpr int kRmsChunks = 4;
+
+template <int kRec, int kW>
+__global__ void __launch_bounds__(256, 4) k_rmsnorm_quant(const uint16_t* __restrict__ x,
+                                                          const uint16_t* __restrict__ gamma, int64_t M, int64_t K,
+                                                          int64_t ld, float eps, uint16_t* __restrict__ y,
+                                                          int64_t ldy, float* __restrict__ rstd_out,
+                                                          uint8_t* __restrict__ codes, void* __restrict__ scales) {
+    __shared__ float part[8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int seg = warp % kW;
+    const int64_t r = (int64_t)blockIdx.x * (8 / kW) + warp / kW;
+    const bool row_ok = r < M;
+    const int64_t k0 = (int64_t)seg * 256 * kRmsChunks + 8 * lane;
     const uint16_t* xr = x + r * ld;
-    uint4 v[kChunks];
+    uint4 v[kRmsChunks];
 #pragma unroll
-    for (int j = 0; j < kChunks; ++j) {
-        const int64_t k = 256 * j + 8 * lane;
-        v[j] = k < K ? ld_stream_v4(xr + k) : make_uint4(0, 0, 0, 0);
-    }
+    for (int j = 0; j < kRmsChunks; ++j)
+        v[j] = (row_ok && k0 + 256 * j < K) ? ld_stream_v4(xr + k0 + 256 * j) : make_uint4(0, 0, 0, 0);
     float ss = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kChunks; ++j) {
+    for (int j = 0; j < kRmsChunks; ++j) {
         float f[8];
         unpack8(v[j], f);
 #pragma unroll
@@ -118,20 +154,34 @@ __global__ void __launch_bounds__(256, kChunks <= 8 ? 2 : 1) k_rmsnorm_quant(con
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    if (kW > 1) {
+        if (lane == 0) part[warp] = ss;
+        __syncthreads();
+        const int w0 = warp - seg;
+        ss = part[w0];
+#pragma unroll
+        for (int i = 1; i < kW; ++i) ss = __fadd_rn(ss, part[w0 + i]);
+    }
+    if (!row_ok) return;
     const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps));
-    if (rstd_out != nullptr && lane == 0) rstd_out[r] = rs;
+    if (rstd_out != nullptr && seg == 0 && lane == 0) rstd_out[r] = rs;
     const int64_t atoms_k = (K + 127) / 128;
     const int sub = lane & 15;
 #pragma unroll
-    for (int j = 0; j < kChunks; ++j) {
-        const int64_t k = 256 * j + 8 * lane;
-        if (256 * j >= K) break;                         // warp-uniform
-        const bool ok = k < K;                           // false only for the upper half of a last half chunk
+    for (int j = 0; j < kRmsChunks; ++j) {
+        const int64_t k = k0 + 256 * j;
+        if (k - 8 * lane >= K) break;                    // warp-uniform: the chunk is empty
+        const bool ok = k < K;                           // false only for the upper half of a half chunk
         float f[8], gm[8];
         unpack8(v[j], f);
-        unpack8(ok ? *reinterpret_cast<const uint4*>(sgamma + k) : make_uint4(0, 0, 0, 0), gm);
+        unpack8(ok ? __ldg(reinterpret_cast<const uint4*>(gamma + k)) : make_uint4(0, 0, 0, 0), gm);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(__fmul_rn(f[i], rs), gm[i]);
+        for (int i = 0; i < 8; i += 2) {
+            const float2 t = mul2(mul2(make_float2(f[i], f[i + 1]), make_float2(rs, rs)),
+                                  make_float2(gm[i], gm[i + 1]));
+            f[i] = t.x;
+            f[i + 1] = t.y;
+        }
         const uint4 w = round8_bf16(f);
         if (y != nullptr && ok) *reinterpret_cast<uint4*>(y + r * ldy + k) = w;
         quant_group16<kRec>(f, ok, sub, r, k / 128, M, atoms_k, codes + r * K + k, scales);
@@ -142,17 +192,31 @@ __global__ void __launch_bounds__(256, kChunks <= 8 ? 2 : 1) k_rmsnorm_quant(con
 // SwiGLU + quantization.  gu [M][ld] holds the gate projection in columns
 // [0, F) and the up projection in [F, 2F); h = RN_bf16(silu(g) u) with
 // silu(g) = g sigmoid(g), sigmoid from e = exp(-|g|) as 1/(1+e) for g >= 0
-// and e/(1+e) for g < 0 (no overflow for large |g|).  Work unit = one
+// and e/(1+e) for g < 0 (no overflow for large |g|); h is within one bf16
+// step of the exact value.  Work unit = one
 // 128-element group of one row (16 lanes); a 256-thread block takes 16 units
 // per round, 4 rounds with all loads issued first.
 // ---------------------------------------------------------------------------
 constexpr int kSwRounds = 4;
 
-__device__ __forceinline__ float silu_times(float g, float u) {
-    const float e = expf(-fabsf(g));
-    const float d = __fadd_rn(1.0f, e);
-    const float sg = __fdiv_rn(g >= 0.0f ? 1.0f : e, d);
-    return __fmul_rn(__fmul_rn(g, sg), u);
+// silu(g) u for 8 pairs in fp32: sigmoid(g) = 1 / (1 + 2^(-g log2 e)) with
+// the hardware base-2 exponential and reciprocal approximations (relative
+// error below 2^-17 for |g| < 90, against the 2^-9 that would move the
+// bf16 result by more than one step), two lanes per packed instruction.
+// Below g = -80 the reciprocal of 1 + e would leave the normal range, so
+// that (rare) tail is recomputed as e/(1+e) with e = expf(g), in a branch
+// taken only by threads that hold such a value.
+__device__ __forceinline__ void silu_times8(float (&g)[8], const float (&u)[8]) {
+    constexpr float kNegLog2e = -1.4426950408889634f;
+#pragma unroll
+    for (int q = 0; q < 8; q += 2) {
+        const float2 t = mul2(make_float2(g[q], g[q + 1]), make_float2(kNegLog2e, kNegLog2e));
+        const float2 d = add2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), make_float2(1.0f, 1.0f));
+        const float2 sg = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+        const float2 h = mul2(mul2(make_float2(g[q], g[q + 1]), sg), make_float2(u[q], u[q + 1]));
+        g[q] = h.x;
+        g[q + 1] = h.y;
+    }
 }
 
 template <int kRec>
@@ -162,29 +226,53 @@ __global__ void __launch_bounds__(256) k_swiglu_quant(const uint16_t* __restrict
     const int64_t G = F / 128, units = M * G;
     const int sub = threadIdx.x & 15;
     const int64_t atoms_k = (F + 127) / 128;
+    const int64_t unit0 = (int64_t)blockIdx.x * kSwRounds * 16 + (threadIdx.x >> 4);
+    // (row, group) of each round's unit: one division, then steps of 16 units
+    int64_t rr[kSwRounds], gg[kSwRounds];
+    rr[0] = unit0 / G;
+    gg[0] = unit0 - rr[0] * G;
+#pragma unroll
+    for (int i = 1; i < kSwRounds; ++i) {
+        rr[i] = rr[i - 1];
+        gg[i] = gg[i - 1] + 16;
+        while (gg[i] >= G) {
+            gg[i] -= G;
+            ++rr[i];
+        }
+    }
     uint4 vg[kSwRounds], vu[kSwRounds];
 #pragma unroll
     for (int i = 0; i < kSwRounds; ++i) {
-        const int64_t u = ((int64_t)blockIdx.x * kSwRounds + i) * 16 + (threadIdx.x >> 4);
-        if (u < units) {
-            const int64_t r = u / G, k = (u % G) * 128 + 8 * sub;
-            vg[i] = ld_stream_v4(gu + r * ld + k);
-            vu[i] = ld_stream_v4(gu + r * ld + F + k);
+        if (unit0 + 16 * i < units) {
+            const uint16_t* p = gu + rr[i] * ld + gg[i] * 128 + 8 * sub;
+            vg[i] = ld_stream_v4(p);
+            vu[i] = ld_stream_v4(p + F);
         } else {
             vg[i] = vu[i] = make_uint4(0, 0, 0, 0);
         }
     }
 #pragma unroll
     for (int i = 0; i < kSwRounds; ++i) {
-        const int64_t u = ((int64_t)blockIdx.x * kSwRounds + i) * 16 + (threadIdx.x >> 4);
-        if (((int64_t)blockIdx.x * kSwRounds + i) * 16 >= units) break;   // block-uniform
-        const bool ok = u < units;
-        const int64_t r = ok ? u / G : 0, g = ok ? u % G : 0, k = g * 128 + 8 * sub;
+        if (unit0 - (threadIdx.x >> 4) + 16 * i >= units) break;   // block-uniform
+        const bool ok = unit0 + 16 * i < units;
+        const int64_t r = ok ? rr[i] : 0, g = ok ? gg[i] : 0, k = g * 128 + 8 * sub;
         float fg[8], fu[8];
         unpack8(vg[i], fg);
         unpack8(vu[i], fu);
+        const float gmin = fminf(fminf(fminf(fg[0], fg[1]), fminf(fg[2], fg[3])),
+                                 fminf(fminf(fg[4], fg[5]), fminf(fg[6], fg[7])));
+        float gsave[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) fg[q] = silu_times(fg[q], fu[q]);
+        for (int q = 0; q < 8; ++q) gsave[q] = fg[q];
+        silu_times8(fg, fu);
+        if (gmin < -80.0f) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (gsave[q] < -80.0f) {
+                    const float e = expf(gsave[q]);
+                    fg[q] = __fmul_rn(__fmul_rn(gsave[q], __fdiv_rn(e, __fadd_rn(1.0f, e))), fu[q]);
+                }
+        }
         const uint4 w = round8_bf16(fg);
         if (h != nullptr && ok) *reinterpret_cast<uint4*>(h + r * ldh + k) = w;
         quant_group16<kRec>(fg, ok, sub, r, g, M, atoms_k, codes + r * F + k, scales);
@@ -195,15 +283,14 @@ template <int kRec>
 cudaError_t launch_rmsnorm_rec(const uint16_t* x, const uint16_t* gamma, int64_t M, int64_t K, int64_t ld, float eps,
                                uint16_t* y, int64_t ldy, float* rstd, uint8_t* codes, void* scales,
                                cudaStream_t st) {
-    const unsigned blocks = (unsigned)((M + 7) / 8);
-    const int chunks = (int)((K + 255) / 256);
-#define FP8BS_RMS(C) k_rmsnorm_quant<kRec, C><<<blocks, 256, 0, st>>>(x, gamma, M, K, ld, eps, y, ldy, rstd, codes, scales)
-    if (chunks <= 1) FP8BS_RMS(1);
-    else if (chunks <= 2) FP8BS_RMS(2);
-    else if (chunks <= 4) FP8BS_RMS(4);
-    else if (chunks <= 8) FP8BS_RMS(8);
-    else if (chunks <= 16) FP8BS_RMS(16);
-    else FP8BS_RMS(32);
+    const int64_t segs = (K + 256 * kRmsChunks - 1) / (256 * kRmsChunks);
+    const int w = segs <= 1 ? 1 : segs <= 2 ? 2 : segs <= 4 ? 4 : 8;
+    const unsigned blocks = (unsigned)((M + (8 / w) - 1) / (8 / w));
+#define FP8BS_RMS(W) k_rmsnorm_quant<kRec, W><<<blocks, 256, 0, st>>>(x, gamma, M, K, ld, eps, y, ldy, rstd, codes, scales)
+    if (w == 1) FP8BS_RMS(1);
+    else if (w == 2) FP8BS_RMS(2);
+    else if (w == 4) FP8BS_RMS(4);
+    else FP8BS_RMS(8);
 #undef FP8BS_RMS
     return cudaGetLastError();
 }
