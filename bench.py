@@ -391,10 +391,23 @@ def _case_quant(kind):
             W = synth.mlp().tensors["W"].to(dev)
             q = fp8.quantize_block(W)
             return lambda: fp8.quantize_block(W, out=q), None
+        if kind == "block_t":
+            W = synth.backward().tensors["W"].to(dev)
+            q, qt = fp8.quantize_block(W, True)
+            return lambda: fp8.quantize_block(W, True, out=q, out_t=qt), None
         if kind == "group_m":
             X = synth.backward().tensors["X"].to(dev)
             q = fp8.quantize_group(X, "M")
             return lambda: fp8.quantize_group(X, "M", out=q), None
+        if kind in ("sync_pack", "sync_install"):
+            W = synth.mlp().tensors["W"].to(dev)
+            qw = fp8.quantize_block(W)
+            payload = fp8.sync_pack([fp8.SyncEntry(1, qw)])
+            if kind == "sync_pack":
+                return lambda: fp8.sync_pack([fp8.SyncEntry(1, qw)], payload=payload), None
+            dst = fp8.QTensor(torch.empty_like(qw.codes), torch.empty_like(qw.scales), qw.rows, qw.cols, qw.recipe,
+                              qw.layout)
+            return lambda: fp8.sync_install(payload, [fp8.SyncEntry(1, dst)], check=False), None
         if kind in ("rmsnorm", "swiglu"):
             if kind == "rmsnorm":
                 X = synth.mlp().tensors["X"].to(dev)
@@ -429,9 +442,10 @@ KERNEL_CASES = {
     "quant_group_1x128": _case_quant("group_k"), "quant_block_128x128": _case_quant("block"),
     "quant_group_128x1_T": _case_quant("group_m"), "quant_mx_1x32": _case_quant("mx"),
     "gemm_mx_dgrad": _case_gemm("mx_dgrad"), "gemm_mx_wgrad": _case_gemm("mx_wgrad"),
-    "quant_mx_32x1_T": _case_quant("mx_t"),
+    "quant_mx_32x1_T": _case_quant("mx_t"), "quant_block_128x128_with_T": _case_quant("block_t"),
     "param_requant": _case_quant("param"), "param_update_requant_with_T": _case_quant("param_update"),
     "rmsnorm_quant": _case_quant("rmsnorm"), "swiglu_quant": _case_quant("swiglu"),
+    "sync_pack": _case_quant("sync_pack"), "sync_install": _case_quant("sync_install"),
 }
 
 

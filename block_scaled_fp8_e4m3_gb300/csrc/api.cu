@@ -731,7 +731,16 @@ fp8_status fp8_sync_install(const void* payload_dev, uint64_t bytes, const fp8_s
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const uint8_t* pay = static_cast<const uint8_t*>(payload_dev);
     std::vector<uint8_t> expect = build_table(dst, n, lay, total);
+    std::vector<CopySeg> segs;
+    for (int32_t i = 0; i < n; ++i) {
+        const EntryLayout& L = lay[(size_t)i];
+        segs.push_back(CopySeg{pay + L.data_off, static_cast<uint8_t*>(dst[i].t.codes), L.data_bytes, 0, 0});
+        if (L.scale_bytes)
+            segs.push_back(CopySeg{pay + L.scale_off, static_cast<uint8_t*>(dst[i].t.scales), L.scale_bytes, 0, 0});
+    }
     cudaError_t e;
+    const ExpectTable* et_ptr = nullptr;
+    unsigned long long tsum = 0;
     if (expect.size() <= (size_t)kMaxExpectBytes) {
         // every byte of header and table except the checksum must match what
         // the destinations imply: checked on the device by the verify kernel
@@ -740,7 +749,8 @@ fp8_status fp8_sync_install(const void* payload_dev, uint64_t bytes, const fp8_s
         static thread_local ExpectTable et;
         et.bytes = (uint32_t)expect.size();
         memcpy(et.data, expect.data(), expect.size());
-        e = launch_sync_verify(pay, expect.size(), total, table_checksum(expect), st, cs, &et);
+        et_ptr = &et;
+        tsum = table_checksum(expect);
     } else {
         std::vector<uint8_t> got(expect.size());
         e = cudaMemcpyAsync(got.data(), pay, got.size(), cudaMemcpyDeviceToHost, cs);
@@ -758,16 +768,16 @@ fp8_status fp8_sync_install(const void* payload_dev, uint64_t bytes, const fp8_s
             }
         }
         put64(&got[32], 0);
-        e = launch_sync_verify(pay, expect.size(), total, table_checksum(got), st, cs);
+        tsum = table_checksum(got);
     }
+    // one cooperative kernel (verify, grid barrier, copy) when the device
+    // runs it and the segments fit one table; otherwise verify, then copy
+    e = launch_sync_install(pay, expect.size(), total, tsum, st, et_ptr, segs.data(), (int)segs.size(), cs);
+    if (e == cudaSuccess) return FP8_OK;
+    if (e != cudaErrorNotSupported && e != cudaErrorCooperativeLaunchTooLarge) return cuda_fail(e, "sync_install");
+    (void)cudaGetLastError();
+    e = launch_sync_verify(pay, expect.size(), total, tsum, st, cs, et_ptr);
     if (e != cudaSuccess) return cuda_fail(e, "sync_install verify");
-    std::vector<CopySeg> segs;
-    for (int32_t i = 0; i < n; ++i) {
-        const EntryLayout& L = lay[(size_t)i];
-        segs.push_back(CopySeg{pay + L.data_off, static_cast<uint8_t*>(dst[i].t.codes), L.data_bytes, 0, 0});
-        if (L.scale_bytes)
-            segs.push_back(CopySeg{pay + L.scale_off, static_cast<uint8_t*>(dst[i].t.scales), L.scale_bytes, 0, 0});
-    }
     for (size_t b = 0; b < segs.size(); b += kMaxCopySegs) {
         const int cnt = (int)std::min<size_t>(kMaxCopySegs, segs.size() - b);
         e = launch_sync_scatter(&segs[b], cnt, st, cs);

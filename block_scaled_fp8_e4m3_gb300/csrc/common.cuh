@@ -32,7 +32,7 @@ struct StatusBlock {
     unsigned int blocks_done;    // blocks of the verify kernel that finished
     unsigned int verdict;        // 0: payload verified, 1: mismatch
     unsigned int header_bad;     // set by fp8_sync_install's device-side header/table check
-    unsigned int reserved32;
+    unsigned int barrier_gen;    // generation of the install kernel's grid barrier
     unsigned long long reserved[3];
 };
 

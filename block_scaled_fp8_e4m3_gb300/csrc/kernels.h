@@ -92,6 +92,11 @@ struct ExpectTable {
     uint32_t bytes;
     uint8_t data[kMaxExpectBytes];
 };
+// Verify + scatter in one cooperative launch; cudaErrorNotSupported when
+// the device cannot run it (or n > kMaxCopySegs): use the two kernels then.
+cudaError_t launch_sync_install(const uint8_t* payload, uint64_t data_offset, uint64_t total_bytes,
+                                unsigned long long table_sum, StatusBlock* status, const ExpectTable* expect,
+                                const CopySeg* segs, int n, cudaStream_t st);
 cudaError_t launch_sync_verify(const uint8_t* payload, uint64_t data_offset, uint64_t total_bytes,
                                unsigned long long table_sum, StatusBlock* status, cudaStream_t st,
                                const ExpectTable* expect = nullptr);

@@ -66,6 +66,8 @@ __device__ __forceinline__ unsigned long long block_sum(unsigned long long v) {
     return s;  // valid in thread 0
 }
 
+constexpr int kUnroll = 4;
+
 __global__ void __launch_bounds__(256) k_sync_pack(const SegTable tab, unsigned long long* checksum_field) {
     __shared__ uint64_t start[kMaxCopySegs + 1];
     if (threadIdx.x == 0) {
@@ -78,26 +80,45 @@ __global__ void __launch_bounds__(256) k_sync_pack(const SegTable tab, unsigned 
     }
     __syncthreads();
     const uint64_t chunks = start[tab.n];
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     unsigned long long sum = 0;
-    for (uint64_t c = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; c < chunks;
-         c += (uint64_t)gridDim.x * blockDim.x) {
-        const int s = find_seg(start, tab.n, c);
-        const CopySeg& sg = tab.seg[s];
-        const uint64_t off = (c - start[s]) * 16;
-        const uint4 v = load16_tail(sg.src, off, sg.bytes);
-        *reinterpret_cast<uint4*>(sg.dst + off) = v;
-        const unsigned long long w0 = (unsigned long long)v.x | ((unsigned long long)v.y << 32);
-        const unsigned long long w1 = (unsigned long long)v.z | ((unsigned long long)v.w << 32);
-        const unsigned long long i0 = sg.dst_word0 + off / 8;
-        sum += mix64(w0 ^ i0) + mix64(w1 ^ (i0 + 1));
+    // kUnroll chunks per thread and round, all loads issued before any store
+    for (uint64_t c = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; c < chunks; c += kUnroll * stride) {
+        uint4 v[kUnroll];
+        int sidx[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint64_t cc = c + u * stride;
+            if (cc < chunks) {
+                sidx[u] = find_seg(start, tab.n, cc);
+                const CopySeg& sg = tab.seg[sidx[u]];
+                v[u] = load16_tail(sg.src, (cc - start[sidx[u]]) * 16, sg.bytes);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint64_t cc = c + u * stride;
+            if (cc < chunks) {
+                const CopySeg& sg = tab.seg[sidx[u]];
+                const uint64_t off = (cc - start[sidx[u]]) * 16;
+                *reinterpret_cast<uint4*>(sg.dst + off) = v[u];
+                const unsigned long long w0 = (unsigned long long)v[u].x | ((unsigned long long)v[u].y << 32);
+                const unsigned long long w1 = (unsigned long long)v[u].z | ((unsigned long long)v[u].w << 32);
+                const unsigned long long i0 = sg.dst_word0 + off / 8;
+                sum += mix64(w0 ^ i0) + mix64(w1 ^ (i0 + 1));
+            }
+        }
     }
     const unsigned long long bs = block_sum(sum);
     if (threadIdx.x == 0 && bs != 0) atomicAdd(checksum_field, bs);
 }
 
-__global__ void __launch_bounds__(256) k_sync_verify(const uint8_t* __restrict__ payload, uint64_t data_offset,
-                                                     uint64_t total_bytes, unsigned long long table_sum,
-                                                     StatusBlock* st, const __grid_constant__ ExpectTable expect) {
+// Checksum of the data region of the payload (this block's share) and, in
+// block 0, the header/table check; returns the block's partial sum (valid in
+// thread 0).
+__device__ __forceinline__ unsigned long long verify_part(const uint8_t* __restrict__ payload, uint64_t data_offset,
+                                                          uint64_t total_bytes, StatusBlock* st,
+                                                          const ExpectTable& expect) {
     if (blockIdx.x == 0 && expect.bytes != 0) {
         // header and entry table against what the destinations imply (the
         // checksum field, bytes 32..39, is what the data is checked against)
@@ -107,37 +128,54 @@ __global__ void __launch_bounds__(256) k_sync_verify(const uint8_t* __restrict__
         if (__syncthreads_or(bad) && threadIdx.x == 0) atomicExch(&st->header_bad, 1u);
     }
     const uint64_t c0 = data_offset / 16, c1 = total_bytes / 16;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     unsigned long long sum = 0;
-    for (uint64_t c = c0 + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; c < c1;
-         c += (uint64_t)gridDim.x * blockDim.x) {
-        const uint4 v = *reinterpret_cast<const uint4*>(payload + c * 16);
-        const unsigned long long w0 = (unsigned long long)v.x | ((unsigned long long)v.y << 32);
-        const unsigned long long w1 = (unsigned long long)v.z | ((unsigned long long)v.w << 32);
-        sum += mix64(w0 ^ (2 * c)) + mix64(w1 ^ (2 * c + 1));
-    }
-    const unsigned long long bs = block_sum(sum);
-    if (threadIdx.x == 0) {
-        atomicAdd(&st->sum, bs);
-        __threadfence();
-        const unsigned int ticket = atomicAdd(&st->blocks_done, 1u);
-        if (ticket == gridDim.x - 1) {
-            __threadfence();
-            const unsigned long long total = atomicAdd(&st->sum, 0ull) + table_sum;
-            const unsigned long long stored = *reinterpret_cast<const unsigned long long*>(payload + 32);
-            const unsigned int header_bad = atomicExch(&st->header_bad, 0u);
-            const unsigned int bad = (total != stored || header_bad) ? 1u : 0u;
-            st->verdict = bad;
-            if (header_bad) atomicOr(&st->error_bits, kErrBadPayload);
-            else if (bad) atomicOr(&st->error_bits, kErrChecksum);
-            st->sum = 0;
-            st->blocks_done = 0;
-            __threadfence();
+    // the next round's loads are issued before this round is mixed
+    uint64_t c = c0 + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+        if (c + u * stride < c1) v[u] = *reinterpret_cast<const uint4*>(payload + (c + u * stride) * 16);
+    for (; c < c1; c += kUnroll * stride) {
+        uint4 nv[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint64_t cn = c + (kUnroll + u) * stride;
+            if (cn < c1) nv[u] = *reinterpret_cast<const uint4*>(payload + cn * 16);
         }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint64_t cc = c + u * stride;
+            if (cc < c1) {
+                const unsigned long long w0 = (unsigned long long)v[u].x | ((unsigned long long)v[u].y << 32);
+                const unsigned long long w1 = (unsigned long long)v[u].z | ((unsigned long long)v[u].w << 32);
+                sum += mix64(w0 ^ (2 * cc)) + mix64(w1 ^ (2 * cc + 1));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = nv[u];
     }
+    return block_sum(sum);
 }
 
-__global__ void __launch_bounds__(256) k_sync_scatter(const SegTable tab, const StatusBlock* st) {
-    if (*reinterpret_cast<const volatile unsigned int*>(&st->verdict) != 0) return;
+// Thread 0 of the block that finishes last: the verdict from the complete
+// sum, then the accumulator is reset for the next call.
+__device__ __forceinline__ void finish_verdict(const uint8_t* payload, unsigned long long table_sum, StatusBlock* st) {
+    __threadfence();
+    const unsigned long long total = atomicAdd(&st->sum, 0ull) + table_sum;
+    const unsigned long long stored = *reinterpret_cast<const unsigned long long*>(payload + 32);
+    const unsigned int header_bad = atomicExch(&st->header_bad, 0u);
+    const unsigned int bad = (total != stored || header_bad) ? 1u : 0u;
+    st->verdict = bad;
+    if (header_bad) atomicOr(&st->error_bits, kErrBadPayload);
+    else if (bad) atomicOr(&st->error_bits, kErrChecksum);
+    st->sum = 0;
+    st->blocks_done = 0;
+    __threadfence();
+}
+
+// This block's share of the segment copies payload -> destinations.
+__device__ __forceinline__ void scatter_part(const SegTable& tab) {
     __shared__ uint64_t start[kMaxCopySegs + 1];
     if (threadIdx.x == 0) {
         uint64_t acc = 0;
@@ -149,24 +187,107 @@ __global__ void __launch_bounds__(256) k_sync_scatter(const SegTable tab, const 
     }
     __syncthreads();
     const uint64_t chunks = start[tab.n];
-    for (uint64_t c = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; c < chunks;
-         c += (uint64_t)gridDim.x * blockDim.x) {
-        const int s = find_seg(start, tab.n, c);
-        const CopySeg& sg = tab.seg[s];
-        const uint64_t off = (c - start[s]) * 16;
-        const uint4 v = *reinterpret_cast<const uint4*>(sg.src + off);   // payload side: padded, aligned
-        if (off + 16 <= sg.bytes) {
-            *reinterpret_cast<uint4*>(sg.dst + off) = v;
-        } else {
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            for (uint64_t i = 0; off + i < sg.bytes; ++i) sg.dst[off + i] = (uint8_t)(w[i / 4] >> (8 * (i % 4)));
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t c = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; c < chunks; c += kUnroll * stride) {
+        uint4 v[kUnroll];
+        int sidx[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint64_t cc = c + u * stride;
+            if (cc < chunks) {
+                sidx[u] = find_seg(start, tab.n, cc);
+                // payload side: padded to 16 bytes and aligned
+                v[u] = *reinterpret_cast<const uint4*>(tab.seg[sidx[u]].src + (cc - start[sidx[u]]) * 16);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint64_t cc = c + u * stride;
+            if (cc >= chunks) continue;
+            const CopySeg& sg = tab.seg[sidx[u]];
+            const uint64_t off = (cc - start[sidx[u]]) * 16;
+            if (off + 16 <= sg.bytes) {
+                *reinterpret_cast<uint4*>(sg.dst + off) = v[u];
+            } else {
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                for (uint64_t i = 0; off + i < sg.bytes; ++i) sg.dst[off + i] = (uint8_t)(w[i / 4] >> (8 * (i % 4)));
+            }
         }
     }
 }
 
-int grid_for(uint64_t chunks) {
-    uint64_t b = (chunks + 255) / 256;
-    if (b > 152 * 8) b = 152 * 8;
+__global__ void __launch_bounds__(256) k_sync_verify(const uint8_t* __restrict__ payload, uint64_t data_offset,
+                                                     uint64_t total_bytes, unsigned long long table_sum,
+                                                     StatusBlock* st, const __grid_constant__ ExpectTable expect) {
+    const unsigned long long bs = verify_part(payload, data_offset, total_bytes, st, expect);
+    if (threadIdx.x == 0) {
+        atomicAdd(&st->sum, bs);
+        __threadfence();
+        if (atomicAdd(&st->blocks_done, 1u) == gridDim.x - 1) finish_verdict(payload, table_sum, st);
+    }
+}
+
+__global__ void __launch_bounds__(256) k_sync_scatter(const SegTable tab, const StatusBlock* st) {
+    if (*reinterpret_cast<const volatile unsigned int*>(&st->verdict) != 0) return;
+    scatter_part(tab);
+}
+
+// Verify and scatter in one cooperative launch (every block resident): the
+// blocks checksum the payload, meet at a grid barrier kept in the status
+// block, and copy only if the verdict is clean -- no destination byte is
+// written before the whole payload has been verified.  The second read of
+// the payload mostly hits L2.  The barrier wait is bounded: on expiry the
+// block records a timeout (site 40) and copies nothing.
+__global__ void __launch_bounds__(256) k_sync_install(const uint8_t* __restrict__ payload, uint64_t data_offset,
+                                                      uint64_t total_bytes, unsigned long long table_sum,
+                                                      StatusBlock* st, const __grid_constant__ ExpectTable expect,
+                                                      const __grid_constant__ SegTable tab) {
+    __shared__ unsigned int proceed;
+    unsigned int gen0 = 0;
+    if (threadIdx.x == 0) gen0 = *reinterpret_cast<volatile unsigned int*>(&st->barrier_gen);
+    const unsigned long long bs = verify_part(payload, data_offset, total_bytes, st, expect);
+    if (threadIdx.x == 0) {
+        atomicAdd(&st->sum, bs);
+        __threadfence();
+        unsigned int go = 1;
+        if (atomicAdd(&st->blocks_done, 1u) == gridDim.x - 1) {
+            finish_verdict(payload, table_sum, st);
+            atomicExch(&st->barrier_gen, gen0 + 1u);
+        } else {
+            const unsigned long long t0 = global_timer_ns();
+            while (*reinterpret_cast<volatile unsigned int*>(&st->barrier_gen) == gen0) {
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    report_timeout(st, 40);
+                    go = 0;
+                    break;
+                }
+                __nanosleep(64);
+            }
+            __threadfence();
+        }
+        proceed = go && *reinterpret_cast<volatile unsigned int*>(&st->verdict) == 0;
+    }
+    __syncthreads();
+    if (proceed) scatter_part(tab);
+}
+
+// Blocks for a grid-stride copy of `chunks` 16-byte chunks: no more than fit
+// on the device at once (SM count x resident blocks of `kernel`, looked up
+// once per device and kernel), so that no block waits for a second wave.
+template <typename Kernel>
+int grid_for(Kernel kernel, uint64_t chunks) {
+    static int resident[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& r = resident[dev & 63];
+    if (r == 0) {
+        int sms = 0, per_sm = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
+        r = sms * (per_sm > 0 ? per_sm : 1);
+    }
+    uint64_t b = (chunks + 256 * kUnroll - 1) / (256 * kUnroll);
+    if (b > (uint64_t)r) b = (uint64_t)r;
     return b == 0 ? 1 : (int)b;
 }
 
@@ -181,7 +302,7 @@ cudaError_t launch_sync_pack(const CopySeg* segs, int n, unsigned long long* che
         chunks += segs[i].padded / 16;
     }
     if (chunks == 0) return cudaSuccess;
-    k_sync_pack<<<grid_for(chunks), 256, 0, st>>>(tab, checksum_field);
+    k_sync_pack<<<grid_for(k_sync_pack, chunks), 256, 0, st>>>(tab, checksum_field);
     return cudaGetLastError();
 }
 
@@ -189,9 +310,36 @@ cudaError_t launch_sync_verify(const uint8_t* payload, uint64_t data_offset, uin
                                unsigned long long table_sum, StatusBlock* status, cudaStream_t st,
                                const ExpectTable* expect) {
     static const ExpectTable none = {};
-    k_sync_verify<<<grid_for((total_bytes - data_offset) / 16), 256, 0, st>>>(
+    k_sync_verify<<<grid_for(k_sync_verify, (total_bytes - data_offset) / 16), 256, 0, st>>>(
         payload, data_offset, total_bytes, table_sum, status, expect ? *expect : none);
     return cudaGetLastError();
+}
+
+cudaError_t launch_sync_install(const uint8_t* payload, uint64_t data_offset, uint64_t total_bytes,
+                                unsigned long long table_sum, StatusBlock* status, const ExpectTable* expect,
+                                const CopySeg* segs, int n, cudaStream_t st) {
+    static const ExpectTable none = {};
+    static int coop[64] = {}, resident[64] = {};   // per device: 1 supported / 2 not; blocks that fit at once
+    int dev = 0;
+    cudaGetDevice(&dev);
+    dev &= 63;
+    if (coop[dev] == 0) {
+        int attr = 0, sms = 0, per_sm = 0;
+        cudaDeviceGetAttribute(&attr, cudaDevAttrCooperativeLaunch, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_sync_install, 256, 0);
+        resident[dev] = sms * per_sm;
+        coop[dev] = (attr && resident[dev] > 0) ? 1 : 2;
+    }
+    if (n > kMaxCopySegs || coop[dev] != 1) return cudaErrorNotSupported;
+    SegTable tab;
+    tab.n = n;
+    for (int i = 0; i < n; ++i) tab.seg[i] = segs[i];
+    const ExpectTable* et = expect ? expect : &none;
+    const int grid = grid_for(k_sync_install, (total_bytes - data_offset) / 16);
+    void* args[] = {(void*)&payload, (void*)&data_offset, (void*)&total_bytes, (void*)&table_sum, (void*)&status,
+                    (void*)et, (void*)&tab};
+    return cudaLaunchCooperativeKernel((const void*)k_sync_install, dim3(grid), dim3(256), args, 0, st);
 }
 
 cudaError_t launch_sync_scatter(const CopySeg* segs, int n, const StatusBlock* status, cudaStream_t st) {
@@ -203,7 +351,7 @@ cudaError_t launch_sync_scatter(const CopySeg* segs, int n, const StatusBlock* s
         chunks += (segs[i].bytes + 15) / 16;
     }
     if (chunks == 0) return cudaSuccess;
-    k_sync_scatter<<<grid_for(chunks), 256, 0, st>>>(tab, status);
+    k_sync_scatter<<<grid_for(k_sync_scatter, chunks), 256, 0, st>>>(tab, status);
     return cudaGetLastError();
 }
 
