@@ -399,6 +399,13 @@ def _case_quant(kind):
             X = synth.backward().tensors["X"].to(dev)
             q = fp8.quantize_group(X, "M")
             return lambda: fp8.quantize_group(X, "M", out=q), None
+        if kind == "permute":
+            wl = synth.moe()
+            Xe = wl.tensors["X"].to(dev)
+            gather, offsets = wl.tensors["gather"].to(dev), wl.tensors["offsets"].to(dev)
+            qxe = fp8.quantize_mx(Xe)
+            qa = fp8.permute_rows_mx(qxe, gather, offsets)
+            return lambda: fp8.permute_rows_mx(qxe, gather, offsets, out=qa), None
         if kind in ("sync_pack", "sync_install"):
             W = synth.mlp().tensors["W"].to(dev)
             qw = fp8.quantize_block(W)
@@ -445,7 +452,7 @@ KERNEL_CASES = {
     "quant_mx_32x1_T": _case_quant("mx_t"), "quant_block_128x128_with_T": _case_quant("block_t"),
     "param_requant": _case_quant("param"), "param_update_requant_with_T": _case_quant("param_update"),
     "rmsnorm_quant": _case_quant("rmsnorm"), "swiglu_quant": _case_quant("swiglu"),
-    "sync_pack": _case_quant("sync_pack"), "sync_install": _case_quant("sync_install"),
+    "sync_pack": _case_quant("sync_pack"), "sync_install": _case_quant("sync_install"), "permute_rows_mx": _case_quant("permute"),
 }
 
 
