@@ -331,6 +331,10 @@ def breakdown(fp8, synth, dev, flush, pk, reps):
     qa = fp8.permute_rows_mx(qxe, gather, offsets)
     qwe = fp8.quantize_mx(We)
     rows = gather.numel()
+    rec("quant_mx_1x32_moe_x", time_kernel(lambda: fp8.quantize_mx(Xe, out=qxe), flush, reps),
+        bytes_=Xe.numel() * (3 + 1 / 32), workload=f"MoE tokens X {Xe.shape[0]}x{Ke}")
+    rec("quant_mx_1x32_moe_w", time_kernel(lambda: fp8.quantize_mx(We, out=qwe), flush, reps),
+        bytes_=We.numel() * (3 + 1 / 32), workload=f"64 expert weights {G}x{Ne}x{Ke}")
     rec("permute_rows_mx", time_kernel(lambda: fp8.permute_rows_mx(qxe, gather, offsets, out=qa), flush, reps),
         bytes_=2 * rows * Ke + 4 * rows + 2 * rows * Ke / 32, workload=f"{rows} rows x {Ke}")
     Ye = torch.empty((rows, Ne), dtype=torch.bfloat16, device=dev)
