@@ -54,6 +54,23 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of the ranks' values (the slowest rank's time); x as is
+    for one rank."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step: float, ms_per_step: float, world: int) -> float:
+    """Throughput of the whole job: every rank processes its own step, the
+    job's step time is the slowest rank's."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -179,7 +196,7 @@ def make_step(fp8, X, W, dev):
     return step, payload.numel(), (qx, qw, Y, qy, rollout)
 
 
-KERNELS_PER_STEP = 6   # quant X, quant W, GEMM, pack, install verify + scatter
+KERNELS_PER_STEP = 5   # quant X, quant W, GEMM, pack, install (one cooperative launch)
 
 
 def breakdown(fp8, synth, dev, flush, pk, reps):
@@ -624,13 +641,9 @@ def main():
         per_kernel += seg
         total_ms += e[0].elapsed_time(e[5])
     per_kernel /= args.steps
-    ms_step = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(total_ms / args.steps, world, dev)
     flops = 2.0 * M * N * K
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(flops, ms_step, world)
 
     # dominant kernel (the GEMM) against the FP8 dense peak
     fp8_peak = 2.0 * pk["bf16_tflops"]
@@ -696,12 +709,8 @@ def main():
     s_out.wait_event(out_done[e2e_steps - 1])
     t1.record(s_out)
     torch.cuda.synchronize()
-    e2e_ms = t0.elapsed_time(t1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1) / e2e_steps, world, dev)
+    e2e = {"value": whole_job_tflops(flops, e2e_ms, world), "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(Xh.numel() * 2 + Wh.numel() * 2), "d2h_bytes_per_step": int(M * N * 2),
            "ms_per_step": e2e_ms, "steps": e2e_steps,
            "schedule": "double-buffered: copies in (step i+1) and out (step i-1) on their own streams"}
