@@ -132,7 +132,7 @@ class Flusher:
 
 
 def time_kernel(fn, flush, reps, warmup=3):
-    """Average device time (ms) of fn() over reps, L2 flushed before each."""
+    """Median device time (ms) of fn() over reps, L2 flushed before each."""
     for _ in range(warmup):
         flush()
         fn()
@@ -145,7 +145,7 @@ def time_kernel(fn, flush, reps, warmup=3):
         e1.record()
         ts.append((e0, e1))
     torch.cuda.synchronize()
-    return float(np.mean([a.elapsed_time(b) for a, b in ts]))
+    return float(np.median([a.elapsed_time(b) for a, b in ts]))
 
 
 def gemm_traffic():
@@ -354,6 +354,13 @@ def breakdown(fp8, synth, dev, flush, pk, reps):
         bytes_=We.numel() * (3 + 1 / 32), workload=f"64 expert weights {G}x{Ne}x{Ke}")
     rec("permute_rows_mx", time_kernel(lambda: fp8.permute_rows_mx(qxe, gather, offsets, out=qa), flush, reps),
         bytes_=2 * rows * Ke + 4 * rows + 2 * rows * Ke / 32, workload=f"{rows} rows x {Ke}")
+    dsti = wl.tensors["dst_index"].to(dev)
+    qd = fp8.dispatch_quantize_mx(Xe, dsti, offsets, rows)
+    rec("dispatch_quantize_mx", time_kernel(lambda: fp8.dispatch_quantize_mx(Xe, dsti, offsets, rows, out=qd), flush,
+                                            reps),
+        bytes_=Xe.numel() * 2 + rows * Ke * (1 + 1 / 32) + 4 * rows,
+        workload=f"MoE dispatch of X {Xe.shape[0]}x{Ke} to {rows} rows (top-8) fused with the MX quantization")
+    del qd
     Ye = torch.empty((rows, Ne), dtype=torch.bfloat16, device=dev)
     rec("gemm_mx_grouped", time_kernel(lambda: fp8.grouped_gemm(qa, qwe, offsets, Ne, out=Ye), flush, reps),
         flops=2.0 * rows * Ne * Ke, workload=f"64 experts, {rows} rows, {Ne}x{Ke}")
@@ -420,6 +427,13 @@ def _case_quant(kind):
             X = synth.backward().tensors["X"].to(dev)
             q = fp8.quantize_group(X, "M")
             return lambda: fp8.quantize_group(X, "M", out=q), None
+        if kind == "permute_quant":
+            wl = synth.moe()
+            Xe = wl.tensors["X"].to(dev)
+            dsti, offsets = wl.tensors["dst_index"].to(dev), wl.tensors["offsets"].to(dev)
+            rows = wl.tensors["gather"].numel()
+            qd = fp8.dispatch_quantize_mx(Xe, dsti, offsets, rows)
+            return lambda: fp8.dispatch_quantize_mx(Xe, dsti, offsets, rows, out=qd), None
         if kind == "permute":
             wl = synth.moe()
             Xe = wl.tensors["X"].to(dev)
@@ -474,6 +488,7 @@ KERNEL_CASES = {
     "param_requant": _case_quant("param"), "param_update_requant_with_T": _case_quant("param_update"),
     "rmsnorm_quant": _case_quant("rmsnorm"), "swiglu_quant": _case_quant("swiglu"),
     "sync_pack": _case_quant("sync_pack"), "sync_install": _case_quant("sync_install"), "permute_rows_mx": _case_quant("permute"),
+    "dispatch_quantize_mx": _case_quant("permute_quant"),
 }
 
 

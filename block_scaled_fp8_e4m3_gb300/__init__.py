@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "FP8Error", "QTensor", "SyncEntry", "library", "quantize_group", "quantize_block", "quantize_mx",
-    "param_requantize", "rmsnorm_quantize", "swiglu_quantize", "permute_rows_mx", "gemm", "grouped_gemm", "sync_payload_size", "sync_pack", "sync_install", "sync_install_noalloc",
+    "param_requantize", "dispatch_quantize_mx", "rmsnorm_quantize", "swiglu_quantize", "permute_rows_mx", "gemm", "grouped_gemm", "sync_payload_size", "sync_pack", "sync_install", "sync_install_noalloc",
     "status_poll", "mx_scale_bytes", "mx_grouped_scale_bytes",
     "RECIPE_BLOCKWISE", "RECIPE_MX", "RECIPE_BLOCKWISE_POW2", "LAYOUT_GROUP_1x128", "LAYOUT_BLOCK_128x128", "LAYOUT_MX_1x32",
     "LAYOUT_MX_1x32_GROUPED",
@@ -75,6 +75,7 @@ def library() -> C.CDLL:
         "fp8_quantize_mx": [P, I64, I64, I64, TP, S],
         "fp8_quantize_mx_transposed": [P, I64, I64, I64, TP, S],
         "fp8_param_requantize": [P, P, I64, I64, I64, TP, TP, S],
+        "fp8_dispatch_quantize_mx": [P, I64, I64, I64, P, C.c_int32, P, C.c_int32, TP, S],
         "fp8_rmsnorm_quantize": [P, P, I64, I64, I64, C.c_float, P, I64, P, TP, S],
         "fp8_swiglu_quantize": [P, I64, I64, I64, P, I64, TP, S],
         "fp8_permute_rows_mx": [TP, P, P, I32, TP, S],
@@ -325,6 +326,29 @@ def permute_rows_mx(q: QTensor, gather: torch.Tensor, offsets: torch.Tensor, out
     src, dst = q.c(), out.c()
     _check(library().fp8_permute_rows_mx(C.byref(src), gather.data_ptr(), offsets.data_ptr(), G, C.byref(dst),
                                          _stream(stream)))
+    return out
+
+
+def dispatch_quantize_mx(x: torch.Tensor, dst_index: torch.Tensor, offsets: torch.Tensor, total: int,
+                         out: Optional[QTensor] = None, stream=None) -> QTensor:
+    """MoE dispatch fused with the MX quantization: every token row of x is
+    quantized once and written to dst rows dst_index[t, :] (int32 [T, top_k],
+    -1 = dropped) of a total-row grouped MXFP8 tensor."""
+    x = _bf16_2d(x)
+    if dst_index.dtype != torch.int32 or offsets.dtype != torch.int32 or dst_index.dim() != 2:
+        raise FP8Error(1, "dst_index must be int32 [T, top_k], offsets int32")
+    T, K = x.shape
+    if dst_index.shape[0] != T or not dst_index.is_contiguous():
+        raise FP8Error(1, "dst_index must be a contiguous [T, top_k] tensor")
+    G = offsets.numel() - 1
+    dev = _dev(x)
+    out = out or QTensor(torch.empty((total, K), dtype=torch.uint8, device=dev),
+                         torch.empty((mx_grouped_scale_bytes(total, K, G),), dtype=torch.uint8, device=dev),
+                         total, K, RECIPE_MX, LAYOUT_MX_1x32_GROUPED)
+    dst = out.c()
+    _check(library().fp8_dispatch_quantize_mx(x.data_ptr(), T, K, x.stride(0), dst_index.data_ptr(),
+                                              dst_index.shape[1], offsets.data_ptr(), G, C.byref(dst),
+                                              _stream(stream)))
     return out
 
 

@@ -530,6 +530,31 @@ fp8_status fp8_permute_rows_mx(const fp8_tensor* src, const int32_t* gather_dev,
     return e == cudaSuccess ? FP8_OK : cuda_fail(e, "permute_rows_mx");
 }
 
+fp8_status fp8_dispatch_quantize_mx(const void* x_bf16, int64_t T, int64_t K, int64_t ld, const int32_t* dst_index_dev,
+                                    int32_t top_k, const int32_t* m_offsets_dev, int32_t num_groups,
+                                    const fp8_tensor* dst, fp8_stream_t stream) {
+    fp8_status s = check_input(x_bf16, T, K, ld, "x");
+    if (s != FP8_OK) return s;
+    if (dst == nullptr || m_offsets_dev == nullptr || (T > 0 && top_k > 0 && dst_index_dev == nullptr))
+        return fail(FP8_ERR_INVALID_ARG, "NULL argument");
+    if (num_groups < 1 || num_groups > 1024) return fail(FP8_ERR_UNSUPPORTED, "num_groups must be in [1, 1024]");
+    if (top_k < 0 || top_k > 64) return fail(FP8_ERR_UNSUPPORTED, "top_k must be in [0, 64]");
+    if (K % 128 != 0 || K == 0)
+        return fail(FP8_ERR_UNSUPPORTED, "dispatch_quantize needs K %% 128 == 0 and K > 0 (K = %lld)", (long long)K);
+    s = check_out(dst, "dst", FP8_RECIPE_MXFP8, FP8_LAYOUT_MX_1x32_GROUPED, dst->rows, K);
+    if (s != FP8_OK) return s;
+    if ((reinterpret_cast<uintptr_t>(dst_index_dev) & 3u) || (reinterpret_cast<uintptr_t>(m_offsets_dev) & 3u))
+        return fail(FP8_ERR_ALIGNMENT, "dst_index/m_offsets misaligned");
+    fp8_status se;
+    StatusBlock* st = status_block(&se);
+    if (st == nullptr) return se;
+    cudaError_t e = launch_dispatch_quant_mx(
+        static_cast<const uint16_t*>(x_bf16), T, K, ld, dst_index_dev, top_k, m_offsets_dev, num_groups, dst->rows,
+        static_cast<uint8_t*>(dst->codes), static_cast<uint8_t*>(dst->scales),
+        fp8_mx_grouped_scale_bytes(dst->rows, K, num_groups), st, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : cuda_fail(e, "dispatch_quantize_mx");
+}
+
 fp8_status fp8_gemm_blockscaled(const fp8_tensor* A, const fp8_tensor* B, void* D, int64_t ldd, int32_t d_dtype,
                                 int32_t op, const fp8_tensor* d_quant, fp8_stream_t stream) {
     if (A == nullptr || B == nullptr) return fail(FP8_ERR_INVALID_ARG, "A or B is NULL");

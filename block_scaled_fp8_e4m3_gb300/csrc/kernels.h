@@ -26,6 +26,10 @@ cudaError_t launch_param_requant(float* master, const float* delta, int64_t N, i
                                  cudaStream_t st);
 cudaError_t launch_quant_mx_t(const uint16_t* x, int64_t R, int64_t K, int64_t ld, uint8_t* codes_t,
                               uint8_t* scales_t, cudaStream_t st);
+cudaError_t launch_dispatch_quant_mx(const uint16_t* x, int64_t T, int64_t K, int64_t ld, const int32_t* dst_index,
+                                     int top_k, const int32_t* offsets, int32_t G, int64_t total, uint8_t* dst_codes,
+                                     uint8_t* dst_scales, int64_t dst_scale_bytes, StatusBlock* status,
+                                     cudaStream_t st);
 // Padding rows of the last MX atom row (rows >= `rows`) set to zero.
 cudaError_t zero_mx_tail(void* scales, int64_t rows, int64_t cols, cudaStream_t st);
 

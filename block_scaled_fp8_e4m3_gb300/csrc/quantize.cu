@@ -576,6 +576,94 @@ __global__ void __launch_bounds__(256) k_permute_rows_mx(const uint8_t* __restri
     }
 }
 
+// ---------------------------------------------------------------------------
+// MoE dispatch fused with the MX quantization, token-major: every source row
+// (token) is read and quantized once, and its codes and scale words are
+// written to each of its top_k destination rows in the expert-grouped layout
+// (dst row dst_index[t][j]; negative entries are dropped tokens).  One warp
+// per token, 8 tokens per block; a block first stages the group offsets and
+// the groups' atom-row bases (prefix sums of ceil(M_g / 128)) in shared
+// memory.  The row is processed 2048 columns at a time: 8 rounds of 256
+// columns (lane: 8 columns, a 32-block is 4 lanes, a 128-column atom a half
+// warp), all loads of a pass issued first.
+// ---------------------------------------------------------------------------
+constexpr int kDqMaxGroups = 1024;
+
+__global__ void __launch_bounds__(256) k_dispatch_quant_mx(const uint16_t* __restrict__ x, int64_t T, int64_t K,
+                                                           int64_t ld, const int32_t* __restrict__ dst_index,
+                                                           int top_k, const int32_t* __restrict__ offsets, int32_t G,
+                                                           int64_t total, uint8_t* __restrict__ dst_codes,
+                                                           uint8_t* __restrict__ dst_scales, StatusBlock* status) {
+    __shared__ int32_t s_off[kDqMaxGroups + 1];
+    __shared__ int64_t s_pg[kDqMaxGroups + 1];
+    for (int g = threadIdx.x; g <= G; g += blockDim.x) s_off[g] = offsets[g];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int64_t acc = 0;
+        for (int g = 0; g < G; ++g) {
+            s_pg[g] = acc;
+            acc += (s_off[g + 1] - s_off[g] + 127) / 128;
+        }
+        s_pg[G] = acc;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, sub = lane & 15, half = lane >> 4;
+    const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int64_t atoms_k = K / 128;
+    const uint16_t* xr = x + t * ld;
+    const int64_t rounds = K / 256 + ((K & 255) ? 1 : 0);   // K % 128 == 0: a last round may be half
+    for (int64_t r0 = 0; r0 < rounds; r0 += 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int64_t k = (r0 + u) * 256 + 8 * lane;
+            v[u] = (r0 + u < rounds && k < K) ? ld_stream_v4(xr + k) : make_uint4(0, 0, 0, 0);
+        }
+        uint2 c[8];
+        uint32_t sw[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            float f[8];
+            unpack8(v[u], f);
+            float a = amax8(f);
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            const int e = mx_exponent(a);
+            c[u] = encode8_mul(f, exp2_int(-e));
+            const uint32_t b = (uint32_t)(e + 127);
+            const uint32_t b1 = __shfl_sync(0xffffffffu, b, 16 * half + 4);
+            const uint32_t b2 = __shfl_sync(0xffffffffu, b, 16 * half + 8);
+            const uint32_t b3 = __shfl_sync(0xffffffffu, b, 16 * half + 12);
+            sw[u] = b | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        }
+        for (int j = 0; j < top_k; ++j) {
+            const int64_t d = dst_index[t * top_k + j];
+            if (d < 0) continue;                                  // dropped token (warp-uniform)
+            if (d >= total) {
+                if (lane == 0) atomicOr(&status->error_bits, kErrDeviceArg);
+                continue;
+            }
+            int lo = 0, hi = G;  // group of row d: last g with offsets[g] <= d
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_off[mid] <= d) lo = mid; else hi = mid;
+            }
+            const int64_t l = d - s_off[lo];
+            uint8_t* srow = dst_scales + (s_pg[lo] + (l >> 7)) * atoms_k * 512 + (l & 31) * 16 + ((l & 127) >> 5) * 4;
+            uint8_t* crow = dst_codes + d * K;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t k = (r0 + u) * 256 + 8 * lane;
+                if (r0 + u < rounds && k < K) {
+                    *reinterpret_cast<uint2*>(crow + k) = c[u];
+                    if (sub == 0) *reinterpret_cast<uint32_t*>(srow + (k / 128) * 512) = sw[u];
+                }
+            }
+        }
+    }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -674,6 +762,18 @@ cudaError_t launch_permute_rows_mx(const uint8_t* src_codes, const uint8_t* src_
     const int64_t blocks = (total + 7) / 8;
     k_permute_rows_mx<<<(unsigned)blocks, 256, 0, st>>>(src_codes, src_scales, src_rows, K, gather, offsets, G, total,
                                                         dst_codes, dst_scales, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_quant_mx(const uint16_t* x, int64_t T, int64_t K, int64_t ld, const int32_t* dst_index,
+                                     int top_k, const int32_t* offsets, int32_t G, int64_t total, uint8_t* dst_codes,
+                                     uint8_t* dst_scales, int64_t dst_scale_bytes, StatusBlock* status,
+                                     cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(dst_scales, 0, (size_t)dst_scale_bytes, st);
+    if (e != cudaSuccess || T == 0 || top_k == 0) return e;
+    const int64_t blocks = (T + 7) / 8;
+    k_dispatch_quant_mx<<<(unsigned)blocks, 256, 0, st>>>(x, T, K, ld, dst_index, top_k, offsets, G, total, dst_codes,
+                                                          dst_scales, status);
     return cudaGetLastError();
 }
 

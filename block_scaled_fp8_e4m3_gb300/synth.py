@@ -105,7 +105,9 @@ def backward() -> Workload:
 def moe_routing(gen: torch.Generator, tokens: int, experts: int, top_k: int, zipf_s: float):
     """Top-k routing with Zipf expert popularity.  Returns (gather index into
     the token rows, int32 group offsets [experts+1], per-(token,slot) expert
-    ids).  Rows are ordered by expert, then token (a stable sort)."""
+    ids, int32 [tokens, top_k] destination row of every (token, slot) -- the
+    inverse of gather).  Rows are ordered by expert, then token (a stable
+    sort)."""
     ranks = torch.arange(1, experts + 1, dtype=torch.float64)
     p_rank = ranks.pow(-zipf_s)
     p_rank = p_rank / p_rank.sum()
@@ -122,18 +124,20 @@ def moe_routing(gen: torch.Generator, tokens: int, experts: int, top_k: int, zip
     counts = torch.bincount(flat_expert, minlength=experts)
     offsets = torch.zeros(experts + 1, dtype=torch.int32)
     offsets[1:] = torch.cumsum(counts, 0).to(torch.int32)
-    return gather, offsets, choice
+    dst_index = torch.empty_like(order)
+    dst_index[order] = torch.arange(order.numel())
+    return gather, offsets, choice, dst_index.reshape(tokens, top_k).to(torch.int32)
 
 
 def moe(tokens: int = 16384, experts: int = 64, top_k: int = 8, hidden: int = 2048,
         ffn: int = 1024, seed: int = 4) -> Workload:
     g = _gen(seed)
-    gather, offsets, choice = moe_routing(g, tokens, experts, top_k, 1.1)
+    gather, offsets, choice, dst_index = moe_routing(g, tokens, experts, top_k, 1.1)
     X = normal_bf16((tokens, hidden), 1.0, g)
     W = normal_bf16((experts, ffn, hidden), 0.02, g)
     return Workload(f"MoE grouped MXFP8 {tokens}x{top_k} tokens, {experts} experts, "
                     f"{ffn}x{hidden}", seed,
-                    {"X": X, "W": W, "gather": gather, "offsets": offsets},
+                    {"X": X, "W": W, "gather": gather, "offsets": offsets, "dst_index": dst_index},
                     {"tokens": tokens, "experts": experts, "top_k": top_k})
 
 

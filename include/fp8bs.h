@@ -256,6 +256,24 @@ fp8_status fp8_permute_rows_mx(const fp8_tensor* src, const int32_t* gather_dev,
                                const int32_t* m_offsets_dev, int32_t num_groups,
                                const fp8_tensor* dst, fp8_stream_t stream);
 
+/* MoE dispatch fused with the MX quantization ([Jet-RL] "Kwantisatieschema":
+ * the activation quantization fused with the operator before it), token
+ * major: each bf16 row t of x [T][ld] (first K columns) is read and
+ * quantized (1x32 blocks, E8M0) once, and its codes and scales are written
+ * to dst rows dst_index[t][j], j < top_k, in the expert-grouped layout -- the
+ * same bytes as fp8_quantize_mx followed by fp8_permute_rows_mx with the
+ * inverse index, without the intermediate FP8 copy or re-reading a token
+ * once per expert.
+ *  dst_index_dev: int32 [T][top_k] device; -1 drops the slot; each dst row
+ *                 should be named at most once (rows named by no slot keep
+ *                 their codes, their scales read 0).
+ *  m_offsets_dev, num_groups, dst: as for fp8_permute_rows_mx (dst->cols = K).
+ * Requires K % 128 == 0, 0 <= top_k <= 64.  Out-of-range entries are skipped
+ * on the device and reported as FP8_ERR_INVALID_ARG by fp8_status_poll(). */
+fp8_status fp8_dispatch_quantize_mx(const void* x_bf16, int64_t T, int64_t K, int64_t ld, const int32_t* dst_index_dev,
+                                    int32_t top_k, const int32_t* m_offsets_dev, int32_t num_groups,
+                                    const fp8_tensor* dst, fp8_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* GEMMs                                                                   */
 /* ---------------------------------------------------------------------- */

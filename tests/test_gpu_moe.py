@@ -111,3 +111,58 @@ def test_full_moe_sampled():
     ref, mag = oracle.gemm_ref_sampled(A_deq_src, W_deq, g_np[rows].astype(np.int64), grp * N + cols)
     got = Y[torch.from_numpy(rows).to(DEV), torch.from_numpy(cols).to(DEV)].double().cpu().numpy()
     assert_gemm_close(got, ref, mag, "moe full sampled")
+
+
+def _moe_dispatch_case(tokens, experts, top_k, hidden, seed):
+    wl = synth.moe(tokens=tokens, experts=experts, top_k=top_k, hidden=hidden, ffn=256, seed=seed)
+    return wl.tensors["X"], wl.tensors["gather"], wl.tensors["offsets"], wl.tensors["dst_index"]
+
+
+@pytest.mark.parametrize("tokens,experts,top_k,hidden,seed", [(200, 8, 2, 256, 5), (700, 16, 4, 384, 6),
+                                                             (300, 4, 2, 128, 7), (90, 6, 3, 2304, 8)])
+def test_fused_dispatch_quantization(tokens, experts, top_k, hidden, seed):
+    """dispatch_quantize_mx: the oracle's 1x32 quantization of the gathered
+    rows in the grouped layout, and the same bytes as quantize-then-permute
+    (hidden 384 and 128 leave a half round of 256 columns; 2304 takes two
+    passes of 2048 columns)."""
+    X, gather, offsets, dst_index = _moe_dispatch_case(tokens, experts, top_k, hidden, seed)
+    g_np, off_np = gather.numpy(), offsets.numpy().astype(np.int64)
+    assert np.array_equal(g_np[dst_index.numpy()], np.repeat(np.arange(tokens), top_k).reshape(tokens, top_k))
+    q = fp8.dispatch_quantize_mx(X.to(DEV), dst_index.to(DEV), offsets.to(DEV), gather.numel())
+    cx, sx = oracle_mx(X)
+    assert_bytes_equal(to_np(q.codes), cx[g_np], "fused dispatch codes")
+    assert_bytes_equal(to_np(q.scales), _grouped_oracle_scales(cx, sx, g_np, off_np, hidden), "fused dispatch scales")
+    q2 = fp8.permute_rows_mx(fp8.quantize_mx(X.to(DEV)), gather.to(DEV), offsets.to(DEV))
+    assert torch.equal(q.codes, q2.codes) and torch.equal(q.scales, q2.scales)
+    assert fp8.status_poll() is None
+
+
+def test_fused_dispatch_full_size():
+    wl = synth.moe()
+    X, gather, offsets, dst_index = (wl.tensors[k] for k in ("X", "gather", "offsets", "dst_index"))
+    q = fp8.dispatch_quantize_mx(X.to(DEV), dst_index.to(DEV), offsets.to(DEV), gather.numel())
+    q2 = fp8.permute_rows_mx(fp8.quantize_mx(X.to(DEV)), gather.to(DEV), offsets.to(DEV))
+    assert torch.equal(q.codes, q2.codes) and torch.equal(q.scales, q2.scales)
+    cx, _ = oracle_mx(X)
+    assert_bytes_equal(to_np(q.codes), cx[gather.numpy()], "fused dispatch codes 131072x2048")
+
+
+def test_fused_dispatch_dropped_and_bad_slots():
+    """-1 drops a slot (its row keeps its codes); an index past the end is
+    skipped and reported."""
+    X = synth.random_bf16((4, 128), seed=9)
+    offsets = torch.tensor([0, 2, 4], dtype=torch.int32)
+    dst_index = torch.tensor([[0], [-1], [3], [1]], dtype=torch.int32)
+    out = fp8.QTensor(torch.full((4, 128), 0x5A, dtype=torch.uint8, device=DEV),
+                      torch.empty((fp8.mx_grouped_scale_bytes(4, 128, 2),), dtype=torch.uint8, device=DEV),
+                      4, 128, fp8.RECIPE_MX, fp8.LAYOUT_MX_1x32_GROUPED)
+    fp8.dispatch_quantize_mx(X.to(DEV), dst_index.to(DEV), offsets.to(DEV), 4, out=out)
+    cx, _ = oracle_mx(X)
+    got = to_np(out.codes)
+    assert_bytes_equal(got[[0, 3, 1]], cx[[0, 2, 3]], "dispatched rows")
+    assert np.all(got[2] == 0x5A)                                  # named by no slot
+    assert fp8.status_poll() is None
+    bad = torch.tensor([[0], [7], [3], [1]], dtype=torch.int32)   # 7 >= 4 rows
+    fp8.dispatch_quantize_mx(X.to(DEV), bad.to(DEV), offsets.to(DEV), 4, out=out)
+    with pytest.raises(fp8.FP8Error):
+        fp8.status_poll()
