@@ -121,3 +121,33 @@ def test_full_mlp_weight_round_trip():
     fp8.sync_install(payload, dst)
     assert torch.equal(dst[0].tensor.codes, qw.codes)
     assert torch.equal(dst[0].tensor.scales, qw.scales)
+
+
+def test_many_entries_use_the_two_kernel_path():
+    """30 quantized entries (60 segments, more than one cooperative launch's
+    table of 32, and more than the 24 entries whose header the device checks):
+    the verify + scatter path and the host header check.  The payload equals
+    the oracle's, the round trip is bit-identical, and a corrupted payload
+    writes nothing."""
+    ws = [synth.random_bf16((128, 256), seed=100 + i, std=0.02) for i in range(30)]
+    qs = [fp8.quantize_block(w.to(DEV)) for w in ws]
+    entries = [fp8.SyncEntry(1000 + i, q) for i, q in enumerate(qs)]
+    payload = fp8.sync_pack(entries)
+    specs = []
+    for i, w in enumerate(ws):
+        c, s = oracle_block(w)
+        specs.append(dict(tag=1000 + i, kind=oracle.KIND_FP8, recipe=oracle.RECIPE_BLOCKWISE, rows=128, cols=256,
+                          layout=oracle.LAYOUT_BLOCK_128x128, data=c, scales=s))
+    assert_bytes_equal(payload.cpu().numpy(), oracle.sync_pack(specs), "30-entry payload")
+    dst = _empty_like(entries)
+    fp8.sync_install(payload, dst)
+    for q, d in zip(qs, dst):
+        assert torch.equal(d.tensor.codes, q.codes) and torch.equal(d.tensor.scales, q.scales)
+    bad = payload.clone()
+    bad[bad.numel() - 300] ^= 0x01
+    dst2 = _empty_like(entries)
+    with pytest.raises(fp8.FP8Error) as ei:
+        fp8.sync_install(bad, dst2)
+    assert ei.value.status == 5
+    for d in dst2:
+        assert int(d.tensor.codes.count_nonzero()) == 0
