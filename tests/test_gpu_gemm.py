@@ -163,6 +163,11 @@ def test_full_mlp_forward_sampled():
     _sampled_check(Y, oracle.dequant_group(cx, sx), oracle.dequant_block(cw, sw), "mlp fwd 8192x4096x12288")
     q2 = fp8.quantize_group(Y, "K")
     assert torch.equal(qy.codes, q2.codes) and torch.equal(qy.scales, q2.scales)
+    # the fused 1x128 quantization of Y against the oracle, on sampled rows
+    rows = torch.from_numpy(np.random.default_rng(3).choice(Y.shape[0], 96, replace=False)).to(Y.device)
+    c, s_ = oracle_group_k(Y[rows].cpu())
+    assert_bytes_equal(to_np(qy.codes[rows]), c, "fused codes, sampled rows")
+    assert_bytes_equal(to_np(qy.scales[:, rows].t().contiguous()), np.ascontiguousarray(s_.T), "fused scales, sampled rows")
 
 
 def test_full_backward_sampled():
