@@ -49,6 +49,7 @@ def load():
         "oracle_param_update": (None, [_P, _P, _I64, _I64, _I64]),
         "oracle_quant_block_128x128_f32": (None, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
         "oracle_quant_block_128x128_f32_pow2": (None, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
+        "oracle_requant_1x128_to_128x1_T": (None, [_P, _P, _I64, _I64, _P, _P]),
         "oracle_bf16_round_f64": (C.c_uint16, [C.c_double]),
         "oracle_rmsnorm": (None, [_P, _P, _I64, _I64, _I64, C.c_float, _P, _P]),
         "oracle_swiglu": (None, [_P, _I64, _I64, _I64, _P]),
@@ -240,6 +241,20 @@ def quant_block_128x128_f32(w, transposed: bool = False, pow2: bool = False):
     if transposed:
         return codes, scales, codes_t, scales_t
     return codes, scales
+
+
+# ---------------------------------------------------------------- saved activation -> WGrad operand
+def requant_1x128_to_128x1_T(codes, scales):
+    """The 128x1 transposed quantization of the fp32 dequantization of a
+    1x128-quantized [M, K] tensor: (codes^T [K, M], scales [M/128, K])."""
+    c = np.ascontiguousarray(codes, np.uint8)
+    s = np.ascontiguousarray(scales, np.float32)
+    M, K = c.shape
+    assert s.shape == (K // 128, M)
+    codes_t = np.empty((K, M), np.uint8)
+    scales_t = np.empty((M // 128, K), np.float32)
+    load().oracle_requant_1x128_to_128x1_T(_ptr(c), _ptr(s), M, K, _ptr(codes_t), _ptr(scales_t))
+    return codes_t, scales_t
 
 
 # ---------------------------------------------------------------- fused producers

@@ -584,6 +584,40 @@ void oracle_quant_block_128x128_f32_pow2(const float* w, int64_t N, int64_t K, i
 }
 
 /* ------------------------------------------------------------------------ */
+/* WGrad operand from the saved FP8 activation ([Jet-RL] "Kwantisatieschema": */
+/* the activations kept for the backward pass are stored in FP8, quantized    */
+/* 1x128; WGrad needs its operands in 128x1 groups along M).  Each element is */
+/* dequantized once in fp32, x' = RN(dec(q) * s), and x' is quantized in      */
+/* 128x1 groups with the codes transposed, exactly as bf16 inputs are.        */
+/* codes [M][K] with 1x128 scales [K/128][M] -> codesT [K][M], scalesT        */
+/* [M/128][K].  M % 128 == 0, K % 128 == 0.                                   */
+/* ------------------------------------------------------------------------ */
+void oracle_requant_1x128_to_128x1_T(const uint8_t* codes, const float* scales, int64_t M, int64_t K,
+                                     uint8_t* codesT, float* scalesT)
+{
+    int64_t B = M / 128;
+    #pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < K; ++c) {
+        float col[128];
+        for (int64_t b = 0; b < B; ++b) {
+            float amax = 0.0f;
+            for (int64_t i = 0; i < 128; ++i) {
+                int64_t m = b * 128 + i;
+                /* dec(q) has at most 4 significant bits: the fp64 product is
+                 * exact, so the cast rounds it once to fp32 */
+                col[i] = (float)(oracle_e4m3_decode(codes[m * K + c]) * (double)scales[(c / 128) * M + m]);
+                float a = fabsf(col[i]);
+                if (a > amax) amax = a;
+            }
+            float s = group_scale(amax);
+            scalesT[b * K + c] = s;
+            for (int64_t i = 0; i < 128; ++i)
+                codesT[c * M + b * 128 + i] = encode_div(col[i], s);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Producers fused with the quantization ([P3] "Kwantisatieschema": the      */
 /* activations saved for the backward pass are stored in FP8, fused with the */
 /* previous operator; "Implementatie": fused activation / RMSNorm kernels).  */
