@@ -303,6 +303,11 @@ def breakdown(fp8, synth, dev, flush, pk, reps):
     Mb, Nb, Kb = 8192, 4096, 4096
     rec("quant_group_128x1_T", time_kernel(lambda: fp8.quantize_group(Xb, "M", out=q_xt), flush, reps),
         bytes_=Mb * Kb * (3 + 4 / 128), workload="X 8192x4096 -> X^T")
+    q_x1 = fp8.quantize_group(Xb, "K")
+    q_xr = fp8.requantize_transposed(q_x1)
+    rec("requant_1x128_to_128x1_T", time_kernel(lambda: fp8.requantize_transposed(q_x1, out=q_xr), flush, reps),
+        bytes_=Mb * Kb * (2 + 8 / 128), workload="saved FP8 X 8192x4096 (1x128) -> X^T 128x1")
+    del q_x1, q_xr
     rec("quant_block_128x128_with_T", time_kernel(lambda: fp8.quantize_block(Wb, True, out=q_w, out_t=q_wt),
                                                   flush, reps),
         bytes_=Nb * Kb * (4 + 8 / 16384), workload="W 4096x4096 + transposed copy")
@@ -419,6 +424,11 @@ def _case_quant(kind):
             W = synth.mlp().tensors["W"].to(dev)
             q = fp8.quantize_block(W)
             return lambda: fp8.quantize_block(W, out=q), None
+        if kind == "requant":
+            X = synth.backward().tensors["X"].to(dev)
+            q1 = fp8.quantize_group(X, "K")
+            qr = fp8.requantize_transposed(q1)
+            return lambda: fp8.requantize_transposed(q1, out=qr), None
         if kind == "block_t":
             W = synth.backward().tensors["W"].to(dev)
             q, qt = fp8.quantize_block(W, True)
@@ -484,7 +494,7 @@ KERNEL_CASES = {
     "quant_group_1x128": _case_quant("group_k"), "quant_block_128x128": _case_quant("block"),
     "quant_group_128x1_T": _case_quant("group_m"), "quant_mx_1x32": _case_quant("mx"),
     "gemm_mx_dgrad": _case_gemm("mx_dgrad"), "gemm_mx_wgrad": _case_gemm("mx_wgrad"),
-    "quant_mx_32x1_T": _case_quant("mx_t"), "quant_block_128x128_with_T": _case_quant("block_t"),
+    "quant_mx_32x1_T": _case_quant("mx_t"), "requant_1x128_to_128x1_T": _case_quant("requant"), "quant_block_128x128_with_T": _case_quant("block_t"),
     "param_requant": _case_quant("param"), "param_update_requant_with_T": _case_quant("param_update"),
     "rmsnorm_quant": _case_quant("rmsnorm"), "swiglu_quant": _case_quant("swiglu"),
     "sync_pack": _case_quant("sync_pack"), "sync_install": _case_quant("sync_install"), "permute_rows_mx": _case_quant("permute"),

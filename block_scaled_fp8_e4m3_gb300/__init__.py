@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "FP8Error", "QTensor", "SyncEntry", "library", "quantize_group", "quantize_block", "quantize_mx",
-    "param_requantize", "dispatch_quantize_mx", "rmsnorm_quantize", "swiglu_quantize", "permute_rows_mx", "gemm", "grouped_gemm", "sync_payload_size", "sync_pack", "sync_install", "sync_install_noalloc",
+    "param_requantize", "requantize_transposed", "dispatch_quantize_mx", "rmsnorm_quantize", "swiglu_quantize", "permute_rows_mx", "gemm", "grouped_gemm", "sync_payload_size", "sync_pack", "sync_install", "sync_install_noalloc",
     "status_poll", "mx_scale_bytes", "mx_grouped_scale_bytes",
     "RECIPE_BLOCKWISE", "RECIPE_MX", "RECIPE_BLOCKWISE_POW2", "LAYOUT_GROUP_1x128", "LAYOUT_BLOCK_128x128", "LAYOUT_MX_1x32",
     "LAYOUT_MX_1x32_GROUPED",
@@ -75,6 +75,7 @@ def library() -> C.CDLL:
         "fp8_quantize_mx": [P, I64, I64, I64, TP, S],
         "fp8_quantize_mx_transposed": [P, I64, I64, I64, TP, S],
         "fp8_param_requantize": [P, P, I64, I64, I64, TP, TP, S],
+        "fp8_requantize_transposed": [TP, TP, S],
         "fp8_dispatch_quantize_mx": [P, I64, I64, I64, P, C.c_int32, P, C.c_int32, TP, S],
         "fp8_rmsnorm_quantize": [P, P, I64, I64, I64, C.c_float, P, I64, P, TP, S],
         "fp8_swiglu_quantize": [P, I64, I64, I64, P, I64, TP, S],
@@ -179,6 +180,22 @@ def quantize_group(x: torch.Tensor, axis: str = "K", out: Optional[QTensor] = No
     t = q.c()
     _check(library().fp8_quantize_group(x.data_ptr(), M, K, x.stride(0), ax, C.byref(t), _stream(stream)))
     return q
+
+
+def requantize_transposed(q: QTensor, out: Optional[QTensor] = None, stream=None) -> QTensor:
+    """128x1 transposed quantization (the WGrad operand) of the fp32
+    dequantization of a saved 1x128 FP8 tensor [M, K]: codes [K, M], scales
+    [M/128, K]."""
+    if q.recipe != RECIPE_BLOCKWISE or q.layout != LAYOUT_GROUP_1x128:
+        raise FP8Error(1, "requantize_transposed takes a 1x128 blockwise tensor")
+    M, K = q.rows, q.cols
+    dev = _dev(q.codes)
+    out = out or QTensor(torch.empty((K, M), dtype=torch.uint8, device=dev),
+                         torch.empty((M // 128, K), dtype=torch.float32, device=dev), K, M, RECIPE_BLOCKWISE,
+                         LAYOUT_GROUP_1x128)
+    a, b = q.c(), out.c()
+    _check(library().fp8_requantize_transposed(C.byref(a), C.byref(b), _stream(stream)))
+    return out
 
 
 def quantize_block(w: torch.Tensor, transposed: bool = False, out: Optional[QTensor] = None,

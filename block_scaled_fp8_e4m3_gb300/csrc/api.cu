@@ -365,6 +365,23 @@ fp8_status fp8_quantize_group(const void* x_bf16, int64_t M, int64_t K, int64_t 
     return fail(FP8_ERR_INVALID_ARG, "unknown axis %d", (int)axis);
 }
 
+fp8_status fp8_requantize_transposed(const fp8_tensor* in, const fp8_tensor* out, fp8_stream_t stream) {
+    if (in == nullptr || out == nullptr) return fail(FP8_ERR_INVALID_ARG, "NULL argument");
+    const int64_t M = in->rows, K = in->cols;
+    if (M < 0 || K < 0) return fail(FP8_ERR_INVALID_ARG, "negative size");
+    if (M % 128 != 0 || K % 128 != 0)
+        return fail(FP8_ERR_UNSUPPORTED, "requantize_transposed needs M, K multiples of 128 (M = %lld, K = %lld)",
+                    (long long)M, (long long)K);
+    fp8_status s = check_out(in, "in", FP8_RECIPE_BLOCKWISE_FP32, FP8_LAYOUT_GROUP_1x128, M, K);
+    if (s != FP8_OK) return s;
+    s = check_out(out, "out", FP8_RECIPE_BLOCKWISE_FP32, FP8_LAYOUT_GROUP_1x128, K, M);
+    if (s != FP8_OK) return s;
+    cudaError_t e = launch_requant_group_m(static_cast<const uint8_t*>(in->codes), static_cast<const float*>(in->scales),
+                                           M, K, static_cast<uint8_t*>(out->codes), static_cast<float*>(out->scales),
+                                           reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : cuda_fail(e, "requantize_transposed");
+}
+
 fp8_status fp8_quantize_block(const void* w_bf16, int64_t N, int64_t K, int64_t ld, const fp8_tensor* out,
                               const fp8_tensor* out_t, fp8_stream_t stream) {
     fp8_status s = check_input(w_bf16, N, K, ld, "w");

@@ -30,6 +30,8 @@ cudaError_t launch_dispatch_quant_mx(const uint16_t* x, int64_t T, int64_t K, in
                                      int top_k, const int32_t* offsets, int32_t G, int64_t total, uint8_t* dst_codes,
                                      uint8_t* dst_scales, int64_t dst_scale_bytes, StatusBlock* status,
                                      cudaStream_t st);
+cudaError_t launch_requant_group_m(const uint8_t* codes, const float* scales, int64_t M, int64_t K, uint8_t* codes_t,
+                                   float* scales_t, cudaStream_t st);
 // Padding rows of the last MX atom row (rows >= `rows`) set to zero.
 cudaError_t zero_mx_tail(void* scales, int64_t rows, int64_t cols, cudaStream_t st);
 

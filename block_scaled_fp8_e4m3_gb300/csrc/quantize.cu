@@ -210,6 +210,92 @@ __global__ void __launch_bounds__(256) k_quant_group_m(const uint16_t* __restric
     }
 }
 
+// ---------------------------------------------------------------------------
+// WGrad operand from a saved 1x128 FP8 activation ("Jet-RL", section
+// "Kwantisatieschema": activations are kept in FP8 for the backward pass;
+// WGrad takes 128x1 groups along M): each element is dequantized once in
+// fp32, x' = RN(dec(q) s_row) (the E4M3 -> f16 conversion is exact), and x'
+// is quantized in 128x1 groups with the codes transposed.  The tiling is that
+// of k_quant_group_m (128 rows x 64 columns, one 1x128 scale per row); x' has
+// a full fp32 significand, so scales and quotients are IEEE divisions.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_requant_group_m(const uint8_t* __restrict__ codes, const float* __restrict__ rs,
+                                                         int64_t M, int64_t K, uint8_t* __restrict__ codes_t,
+                                                         float* __restrict__ scales_t) {
+    __shared__ float red[8][64];
+    __shared__ float col_scale[64];
+    __shared__ uint32_t tile[64 * 33];
+
+    const int64_t ctiles = K / 64;
+    const int64_t mb = (int64_t)blockIdx.x / ctiles;
+    const int64_t c0 = ((int64_t)blockIdx.x % ctiles) * 64;
+    const int64_t m0 = mb * 128;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int chunk = t & 7, quad = t >> 3;
+
+    uint2 v[4];
+    float srow[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t m = m0 + quad * 4 + i;
+        v[i] = __ldcs(reinterpret_cast<const uint2*>(codes + m * K + c0 + chunk * 8));
+        srow[i] = __ldg(rs + (c0 / 128) * M + m);
+    }
+    float f[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t w[2] = {v[i].x, v[i].y};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[h >> 1] >> (16 * (h & 1))), __NV_E4M3);
+            const float2 d = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            f[i][2 * h] = __fmul_rn(d.x, srow[i]);
+            f[i][2 * h + 1] = __fmul_rn(d.y, srow[i]);
+        }
+    }
+    float pa[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float a = fmaxf(fmaxf(fmaxf(0.0f, fabsf(f[0][j])), fabsf(f[1][j])), fmaxf(fabsf(f[2][j]), fabsf(f[3][j])));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
+        pa[j] = a;
+    }
+    if (lane < 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) red[warp][chunk * 8 + j] = pa[j];
+    }
+    __syncthreads();
+    if (t < 64) {
+        float a = red[0][t];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w][t]);
+        const float sc = group_scale(a);
+        col_scale[t] = sc;
+        scales_t[mb * K + c0 + t] = sc;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float sc = col_scale[chunk * 8 + j];
+        tile[(chunk * 8 + j) * 33 + quad] =
+            e4m3x2(__fdiv_rn(f[0][j], sc), __fdiv_rn(f[1][j], sc)) |
+            (e4m3x2(__fdiv_rn(f[2][j], sc), __fdiv_rn(f[3][j], sc)) << 16);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int idx = t + 256 * i;
+        const int col = idx >> 3, part = idx & 7;
+        uint4 o;
+        o.x = tile[col * 33 + part * 4 + 0];
+        o.y = tile[col * 33 + part * 4 + 1];
+        o.z = tile[col * 33 + part * 4 + 2];
+        o.w = tile[col * 33 + part * 4 + 3];
+        *reinterpret_cast<uint4*>(codes_t + (c0 + col) * M + m0 + part * 16) = o;
+    }
+}
+
 // Writes a 128x128 code tile held in shared memory (row stride kStride)
 // transposed: thread t (of 256) takes column t%128 and 64 of its rows, and
 // writes them as 64 contiguous bytes of row t%128 of dst (leading dim ld).
@@ -762,6 +848,14 @@ cudaError_t launch_permute_rows_mx(const uint8_t* src_codes, const uint8_t* src_
     const int64_t blocks = (total + 7) / 8;
     k_permute_rows_mx<<<(unsigned)blocks, 256, 0, st>>>(src_codes, src_scales, src_rows, K, gather, offsets, G, total,
                                                         dst_codes, dst_scales, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_requant_group_m(const uint8_t* codes, const float* scales, int64_t M, int64_t K, uint8_t* codes_t,
+                                   float* scales_t, cudaStream_t st) {
+    if (M == 0 || K == 0) return cudaSuccess;
+    const int64_t blocks = (M / 128) * (K / 64);
+    k_requant_group_m<<<(unsigned)blocks, 256, 0, st>>>(codes, scales, M, K, codes_t, scales_t);
     return cudaGetLastError();
 }
 

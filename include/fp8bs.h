@@ -153,6 +153,19 @@ typedef struct {
 fp8_status fp8_quantize_group(const void* x_bf16, int64_t M, int64_t K, int64_t ld,
                               fp8_axis axis, const fp8_tensor* out, fp8_stream_t stream);
 
+/* The WGrad operand from a saved FP8 activation ([Jet-RL]
+ * "Kwantisatieschema": activations kept for the backward pass are stored in
+ * FP8, quantized 1x128; WGrad takes its operands in 128x1 groups along M),
+ * without the bf16 tensor: every element of `in` is dequantized once in
+ * fp32, x' = RN(dec(q) * s), and x' is quantized in 128x1 groups with the
+ * codes transposed -- exactly fp8_quantize_group(AXIS_M) applied to x'.
+ *  in:  FP8_RECIPE_BLOCKWISE_FP32, FP8_LAYOUT_GROUP_1x128, rows M, cols K.
+ *  out: FP8_RECIPE_BLOCKWISE_FP32, FP8_LAYOUT_GROUP_1x128, rows K, cols M
+ *       (codes [K][M], scales fp32 [M/128][K]).
+ * Requires M % 128 == 0, K % 128 == 0.  Scales and quotients are IEEE fp32
+ * divisions (x' has a full fp32 significand). */
+fp8_status fp8_requantize_transposed(const fp8_tensor* in, const fp8_tensor* out, fp8_stream_t stream);
+
 /* 128x128 block quantization of a bf16 weight w [N][ld] (first K columns).
  * [SkyRL] "なぜ強化学習に FP8 が重要なのか": one scale per 128x128 weight block;
  * [Jet-RL] "Kwantisatieschema".  Requires N % 128 == 0, K % 128 == 0.
