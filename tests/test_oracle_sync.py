@@ -165,3 +165,23 @@ def test_naive_off_policy_differs_sync_does_not(orc):
     dst = _empty_like(spec)
     assert orc.sync_install(orc.sync_pack(spec), dst) == 0
     assert np.array_equal(orc.dequant_block(dst[0]["data"], dst[0]["scales"]), trainer)
+
+
+def test_naive_mismatch_figure_on_the_mlp_weight(orc):
+    """[SkyRL] "独立した量子化がポリシーの一貫性を崩す場合": the synthetic analogue of
+    the trainer-vs-rollout mismatch of the naive (BF16 bridge, per-tensor
+    re-quantization) sync, on the dense-MLP weight 12288x4096 ~N(0, 0.02).
+    Reported, not pinned: the pages' 0.038 and 1.4x come from a trained 4B
+    model."""
+    W = synth.mlp().tensors["W"]
+    w = W.double().numpy()
+    cw, sw = orc.quant_block_128x128(synth.bf16_bits(W))
+    naive_codes, s_naive = orc.naive_requant_per_tensor(cw, sw)
+    trainer = orc.dequant_block(cw, sw)
+    rollout = orc.e4m3_decode(naive_codes) * s_naive
+    rel = np.abs(rollout - trainer).mean() / np.abs(trainer).mean()
+    q_err = np.abs(trainer - w).mean() / np.abs(w).mean()
+    print(f"naive sync: mean relative mismatch {rel:.4f}, {rel / q_err:.2f}x the trainer's quantization error, "
+          f"{np.count_nonzero(naive_codes != cw) / cw.size:.4f} of the codes differ")
+    assert 0.01 < rel < 0.05 and 0.5 < rel / q_err < 2.0
+    assert np.count_nonzero(naive_codes != cw) > 0.9 * cw.size
