@@ -217,6 +217,48 @@ def breakdown(fp8, synth, dev, flush, pk, reps):
                      frac=round(tf / fp8_peak, 4), algorithmic_flops=int(flops))
         out[name] = d
 
+    # tiny blockwise configuration (X 128x512, W 512x512): launch-latency bound,
+    # reported without a roofline; the quantize + GEMM part also as one CUDA
+    # graph replay (the sync calls copy a host header, so they stay eager)
+    wl = synth.tiny()
+    Xt, Wt = wl.tensors["X"].to(dev), wl.tensors["W"].to(dev)
+    qxt, qwt = fp8.quantize_group(Xt, "K"), fp8.quantize_block(Wt)
+    Yt = fp8.gemm(qxt, qwt)
+    pt = fp8.sync_pack([fp8.SyncEntry(1, qwt)])
+    rt = fp8.QTensor(torch.empty_like(qwt.codes), torch.empty_like(qwt.scales), qwt.rows, qwt.cols, qwt.recipe,
+                     qwt.layout)
+
+    def tiny_compute():
+        fp8.quantize_group(Xt, "K", out=qxt)
+        fp8.quantize_block(Wt, out=qwt)
+        fp8.gemm(qxt, qwt, out=Yt)
+
+    def tiny_step():
+        tiny_compute()
+        fp8.sync_pack([fp8.SyncEntry(1, qwt)], payload=pt)
+        fp8.sync_install(pt, [fp8.SyncEntry(1, rt)], check=False)
+
+    out["tiny_step_eager"] = {"ms": round(time_kernel(tiny_step, flush, reps), 5), "bound": "launch",
+                              "workload": "X 128x512 1x128, W 512x512 128x128, GEMM 128x512x512, pack + install W"}
+    out["tiny_quant_gemm_eager"] = {"ms": round(time_kernel(tiny_compute, flush, reps), 5), "bound": "launch",
+                                    "workload": "quantize X and W, GEMM 128x512x512"}
+    try:
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            tiny_compute()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            tiny_compute()
+        out["tiny_quant_gemm_graph"] = {"ms": round(time_kernel(graph.replay, flush, reps), 5), "bound": "launch",
+                                        "workload": "the same three kernels replayed as one CUDA graph"}
+        del graph
+    except Exception as e:  # noqa: BLE001 - reported, the rest of the breakdown still runs
+        out["tiny_quant_gemm_graph"] = {"error": str(e).splitlines()[0][:200]}
+    del Xt, Wt, qxt, qwt, Yt, pt, rt
+
     # dense MLP forward + sync
     wl = synth.mlp()
     X, W = wl.tensors["X"].to(dev), wl.tensors["W"].to(dev)
