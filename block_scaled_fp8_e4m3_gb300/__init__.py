@@ -76,6 +76,7 @@ def library() -> C.CDLL:
         "fp8_quantize_mx_transposed": [P, I64, I64, I64, TP, S],
         "fp8_param_requantize": [P, P, I64, I64, I64, TP, TP, S],
         "fp8_requantize_transposed": [TP, TP, S],
+        "fp8_check_wait_expiry": [I64, S],
         "fp8_dispatch_quantize_mx": [P, I64, I64, I64, P, C.c_int32, P, C.c_int32, TP, S],
         "fp8_rmsnorm_quantize": [P, P, I64, I64, I64, C.c_float, P, I64, P, TP, S],
         "fp8_swiglu_quantize": [P, I64, I64, I64, P, I64, TP, S],
@@ -469,6 +470,13 @@ def sync_install_noalloc(payload: torch.Tensor, dst: Sequence[SyncEntry], stream
     mismatch raises FP8Error(FP8_ERR_CHECKSUM)."""
     _check(library().fp8_sync_install_noalloc(payload.data_ptr(), payload.numel(), _entries(dst), len(dst),
                                               _stream(stream)))
+
+
+def check_wait_expiry(limit_ns: int = 20_000_000, stream=None) -> None:
+    """Runs the library's bounded-wait failure path on the device (a wait
+    that nothing completes, given up after limit_ns); the next status_poll()
+    raises FP8Error with FP8_ERR_TIMEOUT."""
+    _check(library().fp8_check_wait_expiry(int(limit_ns), _stream(stream)))
 
 
 def status_poll(stream=None):

@@ -828,6 +828,15 @@ fp8_status fp8_sync_install(const void* payload_dev, uint64_t bytes, const fp8_s
     return FP8_OK;
 }
 
+fp8_status fp8_check_wait_expiry(int64_t limit_ns, fp8_stream_t stream) {
+    if (limit_ns < 1000 || limit_ns > 2000000000) return fail(FP8_ERR_INVALID_ARG, "limit_ns must be in [1 us, 2 s]");
+    fp8_status se;
+    StatusBlock* st = status_block(&se);
+    if (st == nullptr) return se;
+    cudaError_t e = launch_wait_expiry((unsigned long long)limit_ns, st, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : cuda_fail(e, "check_wait_expiry");
+}
+
 fp8_status fp8_status_poll(fp8_stream_t stream) {
     fp8_status se;
     StatusBlock* st = status_block(&se);

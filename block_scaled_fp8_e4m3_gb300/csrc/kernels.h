@@ -103,6 +103,7 @@ struct ExpectTable {
 cudaError_t launch_sync_install(const uint8_t* payload, uint64_t data_offset, uint64_t total_bytes,
                                 unsigned long long table_sum, StatusBlock* status, const ExpectTable* expect,
                                 const CopySeg* segs, int n, cudaStream_t st);
+cudaError_t launch_wait_expiry(unsigned long long limit_ns, StatusBlock* status, cudaStream_t st);
 cudaError_t launch_sync_verify(const uint8_t* payload, uint64_t data_offset, uint64_t total_bytes,
                                unsigned long long table_sum, StatusBlock* status, cudaStream_t st,
                                const ExpectTable* expect = nullptr);

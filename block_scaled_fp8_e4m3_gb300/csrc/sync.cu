@@ -291,7 +291,34 @@ int grid_for(Kernel kernel, uint64_t chunks) {
     return b == 0 ? 1 : (int)b;
 }
 
+// Diagnostic: one warp waits on a shared-memory mbarrier that nothing will
+// complete, giving up after limit_ns exactly as every bounded wait of the
+// library does (timeout recorded in the status block, site 90), then
+// returns -- the path taken when a peer of a real wait never signals.
+__global__ void k_wait_expiry(unsigned long long limit_ns, StatusBlock* st) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x != 0) return;
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(&bar, 0)) {
+        if (global_timer_ns() - t0 > limit_ns) {
+            report_timeout(st, 90);
+            return;
+        }
+        __nanosleep(1000);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_expiry(unsigned long long limit_ns, StatusBlock* status, cudaStream_t st) {
+    k_wait_expiry<<<1, 32, 0, st>>>(limit_ns, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_sync_pack(const CopySeg* segs, int n, unsigned long long* checksum_field, cudaStream_t st) {
     SegTable tab;

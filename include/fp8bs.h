@@ -405,6 +405,14 @@ fp8_status fp8_sync_install_noalloc(const void* payload_dev, uint64_t bytes, con
 /* Status and diagnostics                                                  */
 /* ---------------------------------------------------------------------- */
 
+/* Diagnostic of the failure path shared by every bounded on-device wait:
+ * launches one warp that waits on a barrier nothing will complete and gives
+ * up after limit_ns (1 us .. 2 s), recording FP8_ERR_TIMEOUT in the status
+ * block as a real wait whose peer never signals does.  The next
+ * fp8_status_poll() returns FP8_ERR_TIMEOUT and clears it; the context stays
+ * usable.  No fault, trap or hang is involved. */
+fp8_status fp8_check_wait_expiry(int64_t limit_ns, fp8_stream_t stream);
+
 /* Synchronizes `stream`, reads and clears the current device's status
  * block.  Returns FP8_OK, FP8_ERR_CHECKSUM, FP8_ERR_TIMEOUT or
  * FP8_ERR_INVALID_ARG (device-detected), or FP8_ERR_CUDA. */
