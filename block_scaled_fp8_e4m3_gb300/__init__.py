@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "FP8Error", "QTensor", "SyncEntry", "library", "quantize_group", "quantize_block", "quantize_mx",
     "param_requantize", "requantize_transposed", "dispatch_quantize_mx", "rmsnorm_quantize", "swiglu_quantize", "permute_rows_mx", "gemm", "grouped_gemm", "sync_payload_size", "sync_pack", "sync_install", "sync_install_noalloc",
-    "status_poll", "mx_scale_bytes", "mx_grouped_scale_bytes",
+    "status_poll", "check_wait_expiry", "mx_scale_bytes", "mx_grouped_scale_bytes",
     "RECIPE_BLOCKWISE", "RECIPE_MX", "RECIPE_BLOCKWISE_POW2", "LAYOUT_GROUP_1x128", "LAYOUT_BLOCK_128x128", "LAYOUT_MX_1x32",
     "LAYOUT_MX_1x32_GROUPED",
 ]
