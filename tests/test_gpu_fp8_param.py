@@ -70,6 +70,40 @@ def test_special_values():
         assert_bytes_equal(to_np(q.scales), s, f"scales pow2={pow2}")
 
 
+def _midpoint_band(s_target: float, ulps: int = 10) -> np.ndarray:
+    """fp32 values at and within `ulps` representable steps of s_target times
+    each of the 126 rounding midpoints between adjacent positive E4M3 values,
+    with both signs."""
+    v = oracle.e4m3_decode(np.arange(127, dtype=np.uint8))          # 0 .. 448, ascending
+    base = ((v[:-1] + v[1:]) / 2 * s_target).astype(np.float32).view(np.int32)
+    band = np.concatenate([base + k for k in range(-ulps, ulps + 1)]).view(np.float32)
+    return np.concatenate([band, -band])
+
+
+def test_quotients_at_rounding_midpoints():
+    """fp32 elements whose quotient by a non-power-of-two block scale falls at
+    or beside an E4M3 rounding midpoint: there the product with the reciprocal
+    cannot decide the code, and the codes must still be those of the IEEE
+    quotient (ties to even)."""
+    targets = [1.37, 0.0071, 5.3e4, 3.1e-20, 2.9e15]
+    w = np.zeros((128, 128 * len(targets)), np.float32)
+    for b, st in enumerate(targets):
+        blk = np.zeros(128 * 128, np.float32)
+        band = _midpoint_band(st)
+        blk[0] = np.float32(448.0 * st)            # the block maximum: s = RN(blk[0] / 448), near st
+        blk[1:1 + band.size] = band
+        w[:, 128 * b:128 * (b + 1)] = blk.reshape(128, 128)
+    q, qt = fp8.param_requantize(torch.from_numpy(w).to(DEV), transposed=True)
+    _check(q, qt, w, False, "midpoints")
+    # the band reaches both sides of the midpoints, and it separates the IEEE
+    # quotient from the plain product with RN(1/s)
+    c, sc = oracle.quant_block_128x128_f32(w)
+    assert len(np.unique(c)) > 200
+    r = np.repeat(np.float32(1) / sc.astype(np.float32), 128, axis=1)
+    naive = oracle.e4m3_encode((w * r).astype(np.float32))
+    assert (naive != c).any()
+
+
 @pytest.mark.parametrize("pow2", [False, True])
 def test_trajectory(pow2):
     """30 optimizer steps: the master and Q(W_t) match the oracle after each."""

@@ -51,3 +51,37 @@ def test_wgrad_on_the_requantized_operand():
     c2, s2 = oracle.requant_1x128_to_128x1_T(cx, sx)
     ref, mag = oracle.gemm_ref(oracle.dequant_group(c1, s1), oracle.dequant_group(c2, s2))
     assert_gemm_close(bf16_dev_to_f64(dW), ref, mag, "wgrad on the re-quantized X")
+
+
+def test_quotients_at_rounding_midpoints():
+    """Dequantized values x' whose quotient by the (non-power-of-two) 128x1
+    scale lies at or within 10 ulps of an E4M3 rounding midpoint: the codes of
+    the IEEE quotient, byte for byte.  Block b of 128 rows shifts every row
+    scale by b - 10 ulps; row 0 of each block sets the column maxima."""
+    v = oracle.e4m3_decode(np.arange(127, dtype=np.uint8))
+    mids = (v[:-1] + v[1:]) / 2                                   # 126 midpoints
+    sc = 7.77
+    blocks = 21
+    M, K = 128 * blocks, 256
+    e = -(np.arange(K) % 7)                                       # column j holds +-2^e, e in [-6, 0]
+    col_codes = ((e + 7) << 3).astype(np.uint8) | np.where(np.arange(K) % 2 == 1, 0x80, 0).astype(np.uint8)
+    codes = np.zeros((M, K), np.uint8)
+    srow = np.ones((K // 128, M), np.float32)
+    for b in range(blocks):
+        r0 = 128 * b
+        codes[r0] = 0x7E                                          # 448 * 7.77: the column maximum
+        srow[:, r0] = np.float32(sc)
+        s_mid = ((mids * sc).astype(np.float32).view(np.int32) + (b - 10)).view(np.float32)
+        codes[r0 + 1:r0 + 127] = col_codes
+        srow[:, r0 + 1:r0 + 127] = s_mid
+    q = fp8.QTensor(torch.from_numpy(codes).to(DEV), torch.from_numpy(srow).to(DEV), M, K, fp8.RECIPE_BLOCKWISE,
+                    fp8.LAYOUT_GROUP_1x128)
+    qt = fp8.requantize_transposed(q)
+    ct, st = oracle.requant_1x128_to_128x1_T(codes, srow)
+    assert_bytes_equal(to_np(qt.codes), ct, "codes^T")
+    assert_bytes_equal(to_np(qt.scales), st, "scales")
+    assert len(np.unique(ct)) > 200
+    # the inputs do separate the IEEE quotient from the plain product with RN(1/s)
+    xd = (oracle.e4m3_decode(codes).astype(np.float32) * srow[0][:, None]).astype(np.float32)
+    naive = oracle.e4m3_encode((xd * np.repeat(np.float32(1) / st, 128, axis=0)).astype(np.float32))
+    assert (naive.T != ct).any()
