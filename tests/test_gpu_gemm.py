@@ -194,3 +194,32 @@ def test_full_mx_sampled():
     cx, sx = oracle_mx(X)
     cw, sw = oracle_mx(W)
     _sampled_check(Y, oracle.dequant_mx(cx, sx), oracle.dequant_mx(cw, sw), "mx full")
+
+
+def test_zero_rows_and_mismatched_operands():
+    """A GEMM over zero rows returns an empty D (and an empty fused
+    quantization) for both recipes; operands of different recipes, or a
+    blockwise weight whose N is not a multiple of 128, are rejected before
+    any launch and leave the device status clean."""
+    K, N = 256, 256
+    W = synth.random_bf16((N, K), seed=61, std=0.02).to(DEV)
+    qw, mw = fp8.quantize_block(W), fp8.quantize_mx(W)
+    x0 = torch.empty((0, K), dtype=torch.bfloat16, device=DEV)
+    for qa, qb in ((fp8.quantize_group(x0, "K"), qw), (fp8.quantize_mx(x0), mw)):
+        assert fp8.gemm(qa, qb).shape == (0, N)
+        Y, qy = fp8.gemm(qa, qb, quantize_output=True)
+        assert Y.shape == (0, N) and qy.codes.shape == (0, N)
+    X = synth.random_bf16((128, K), seed=62).to(DEV)
+    qx, mx = fp8.quantize_group(X, "K"), fp8.quantize_mx(X)
+    for a, b in ((qx, mw), (mx, qw)):
+        with pytest.raises(fp8.FP8Error) as err:
+            fp8.gemm(a, b)
+        assert err.value.status == 1
+    w48 = fp8.quantize_mx(synth.random_bf16((48, K), seed=63, std=0.02).to(DEV))
+    qw48 = fp8.QTensor(w48.codes, torch.ones((1, 2), dtype=torch.float32, device=DEV), 48, K,
+                       fp8.RECIPE_BLOCKWISE, fp8.LAYOUT_BLOCK_128x128)
+    with pytest.raises(fp8.FP8Error) as err:
+        fp8.gemm(qx, qw48)
+    assert err.value.status == 3
+    fp8.status_poll()
+    torch.testing.assert_close(fp8.gemm(qx, qw), fp8.gemm(qx, qw))    # still usable afterwards
