@@ -204,13 +204,28 @@ def breakdown(fp8, synth, dev, flush, pk, reps):
     hbm = pk["hbm_gbs"]
     fp8_peak = 2.0 * pk["bf16_tflops"]
     out = {}
+    copy_ms = {}
+
+    def same_size_copy_ms(nbytes):
+        """Device time of a plain tensor copy moving the same bytes (half read,
+        half written): what a launch of this size reaches in practice, as
+        context beside the fraction of the sustained copy bandwidth."""
+        half = (int(nbytes) // 2 + 15) // 16 * 16
+        if half not in copy_ms:
+            src = torch.empty(half, dtype=torch.uint8, device=dev).fill_(3)
+            dst = torch.empty_like(src)
+            copy_ms[half] = time_kernel(lambda: dst.copy_(src), flush, reps)
+            del src, dst
+        return copy_ms[half]
 
     def rec(name, ms, bytes_=None, flops=None, workload=""):
         d = {"ms": round(ms, 5), "workload": workload}
         if bytes_ is not None:
             gbs = bytes_ / (ms * 1e-3) / 1e9
+            cms = same_size_copy_ms(bytes_)
             d.update(bound="hbm", achieved=round(gbs, 1), unit="GB/s", peak=hbm, frac=round(gbs / hbm, 4),
-                     frac_of_8tbs=round(gbs / 8000.0, 4), algorithmic_bytes=int(bytes_))
+                     frac_of_8tbs=round(gbs / 8000.0, 4), algorithmic_bytes=int(bytes_),
+                     same_size_copy_ms=round(cms, 5), frac_of_same_size_copy=round(cms / ms, 4))
         else:
             tf = flops / (ms * 1e-3) / 1e12
             d.update(bound="tensor", achieved=round(tf, 1), unit="TFLOP/s", peak=round(fp8_peak, 1),
