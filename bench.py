@@ -817,7 +817,7 @@ def main():
                 "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "seed": 2,
                            "step": "quant X 1x128, quant W 128x128, GEMM+fused quant of Y, sync pack W, install W",
                            "l2": "flushed between steps (256 MB write, then 256 MB read)",
-                           "parallelism": f"replicas x{world}"},
+                           "parallelism": f"replicas x{world}", "input_sha256": wl.sha256()},
                 "roofline": roofline, "step_kernels": step_kernels, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clocks, "peaks": pk,
                 "kernels": kernels}
