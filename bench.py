@@ -796,6 +796,37 @@ def main():
            "h2d_bytes_per_step": int(Xh.numel() * 2 + Wh.numel() * 2), "d2h_bytes_per_step": int(M * N * 2),
            "ms_per_step": e2e_ms, "steps": e2e_steps,
            "schedule": "double-buffered: copies in (step i+1) and out (step i-1) on their own streams"}
+
+    # the host link alone, for context: the same copies without the kernels
+    def copies_ms(fn, reps=10):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    def h2d():
+        X.copy_(Xp, non_blocking=True)
+        W.copy_(Wp, non_blocking=True)
+
+    def both():
+        cur = torch.cuda.current_stream()
+        s_in.wait_stream(cur)
+        s_out.wait_stream(cur)
+        with torch.cuda.stream(s_in):
+            h2d()
+        with torch.cuda.stream(s_out):
+            Yp.copy_(keep[2], non_blocking=True)
+        cur.wait_stream(s_in)
+        cur.wait_stream(s_out)
+
+    e2e["host_link"] = {"h2d_ms": round(copies_ms(h2d), 4),
+                        "d2h_ms": round(copies_ms(lambda: Yp.copy_(keep[2], non_blocking=True)), 4),
+                        "both_concurrent_ms": round(copies_ms(both), 4)}
     del keep2, X2, W2, sets
 
     kernels = None
