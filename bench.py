@@ -763,35 +763,42 @@ def main():
     s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     e2e_steps = min(args.steps, 20)
     ev = lambda: torch.cuda.Event(enable_timing=False)
-    in_done = [ev() for _ in range(e2e_steps)]
-    comp_done = [ev() for _ in range(e2e_steps)]
-    out_done = [ev() for _ in range(e2e_steps)]
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(s_in)
-    for i in range(e2e_steps):
-        Xb, Wb, stepb = sets[i % 2]
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(comp_done[i - 2])      # step i-2 has finished reading this set
-            Xb.copy_(Xp, non_blocking=True)
-            Wb.copy_(Wp, non_blocking=True)
-            in_done[i].record(s_in)
-        with torch.cuda.stream(s_comp):
-            s_comp.wait_event(in_done[i])
-            if i >= 2:
-                s_comp.wait_event(out_done[i - 2])     # this set's Y has been copied out
-            Y = stepb()
-            comp_done[i].record(s_comp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(comp_done[i])
-            Yp.copy_(Y, non_blocking=True)
-            out_done[i].record(s_out)
-    s_out.wait_event(out_done[e2e_steps - 1])
-    t1.record(s_out)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(t0.elapsed_time(t1) / e2e_steps, world, dev)
+
+    def run_e2e(n):
+        """n pipelined steps; returns the device time from the first input
+        copy to the last output copy (ms)."""
+        in_done = [ev() for _ in range(n)]
+        comp_done = [ev() for _ in range(n)]
+        out_done = [ev() for _ in range(n)]
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(s_in)
+        for i in range(n):
+            Xb, Wb, stepb = sets[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(comp_done[i - 2])      # step i-2 has finished reading this set
+                Xb.copy_(Xp, non_blocking=True)
+                Wb.copy_(Wp, non_blocking=True)
+                in_done[i].record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(in_done[i])
+                if i >= 2:
+                    s_comp.wait_event(out_done[i - 2])     # this set's Y has been copied out
+                Y = stepb()
+                comp_done[i].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[i])
+                Yp.copy_(Y, non_blocking=True)
+                out_done[i].record(s_out)
+        s_out.wait_event(out_done[n - 1])
+        t1.record(s_out)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    run_e2e(max(args.warmup, 3))                           # untimed: both buffer sets in use once
+    e2e_ms = max_over_ranks(run_e2e(e2e_steps) / e2e_steps, world, dev)
     e2e = {"value": whole_job_tflops(flops, e2e_ms, world), "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(Xh.numel() * 2 + Wh.numel() * 2), "d2h_bytes_per_step": int(M * N * 2),
            "ms_per_step": e2e_ms, "steps": e2e_steps,

@@ -220,7 +220,7 @@ __device__ __forceinline__ void silu_times8(float (&g)[8], const float (&u)[8]) 
 }
 
 template <int kRec>
-__global__ void __launch_bounds__(256) k_swiglu_quant(const uint16_t* __restrict__ gu, int64_t M, int64_t F,
+__global__ void __launch_bounds__(256, 4) k_swiglu_quant(const uint16_t* __restrict__ gu, int64_t M, int64_t F,
                                                       int64_t ld, uint16_t* __restrict__ h, int64_t ldh,
                                                       uint8_t* __restrict__ codes, void* __restrict__ scales) {
     const int64_t G = F / 128, units = M * G;

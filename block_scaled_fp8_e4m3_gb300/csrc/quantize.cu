@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(256, 4) k_quant_group_k(const uint16_t* __rest
 // memory (column stride 33 words), which is written out 16 bytes per thread.
 // ---------------------------------------------------------------------------
 template <bool kPow2>
-__global__ void __launch_bounds__(256) k_quant_group_m(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+__global__ void __launch_bounds__(256, 5) k_quant_group_m(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                        int64_t ld, uint8_t* __restrict__ codes_t,
                                                        void* __restrict__ scales) {
     __shared__ float red[8][64];
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(256) k_quant_group_m(const uint16_t* __restric
 // of k_quant_group_m (128 rows x 64 columns, one 1x128 scale per row); x' has
 // a full fp32 significand, so scales and quotients are IEEE divisions.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_requant_group_m(const uint8_t* __restrict__ codes, const float* __restrict__ rs,
+__global__ void __launch_bounds__(256, 5) k_requant_group_m(const uint8_t* __restrict__ codes, const float* __restrict__ rs,
                                                          int64_t M, int64_t K, uint8_t* __restrict__ codes_t,
                                                          float* __restrict__ scales_t) {
     __shared__ float red[8][64];
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(256) k_quant_block(const uint16_t* __restrict_
 // recipe: e from RN(amax/448), codes from the exact product w * 2^-e.
 // ---------------------------------------------------------------------------
 template <bool kPow2, bool kDelta>
-__global__ void __launch_bounds__(256) k_param_requant(float* __restrict__ master, const float* __restrict__ delta,
+__global__ void __launch_bounds__(256, 3) k_param_requant(float* __restrict__ master, const float* __restrict__ delta,
                                                        int64_t N, int64_t K, int64_t ld, uint8_t* __restrict__ codes,
                                                        void* __restrict__ scales, uint8_t* __restrict__ codes_t,
                                                        void* __restrict__ scales_t) {
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(256) k_param_requant(float* __restrict__ maste
 // (shuffle over xor 1, 2).  The atom is assembled in shared memory and
 // written with 16-byte stores.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_quant_mx(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ld,
+__global__ void __launch_bounds__(256, 5) k_quant_mx(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ld,
                                                   uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
     __shared__ __align__(16) uint8_t atom[512];
     const int64_t atoms_k = (K + 127) / 128;
@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(256) k_quant_mx(const uint16_t* __restrict__ x
 // 128 rows.  Codes are the exact products x * 2^-e, transposed through a
 // 33-word-stride shared tile and written 16 bytes per thread.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_quant_mx_t(const uint16_t* __restrict__ x, int64_t R, int64_t K,
+__global__ void __launch_bounds__(256, 6) k_quant_mx_t(const uint16_t* __restrict__ x, int64_t R, int64_t K,
                                                     int64_t ld, uint8_t* __restrict__ codes_t,
                                                     uint8_t* __restrict__ scales_t) {
     __shared__ float red[8][64];
@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(256) k_permute_rows_mx(const uint8_t* __restri
 // ---------------------------------------------------------------------------
 constexpr int kDqMaxGroups = 1024;
 
-__global__ void __launch_bounds__(256) k_dispatch_quant_mx(const uint16_t* __restrict__ x, int64_t T, int64_t K,
+__global__ void __launch_bounds__(256, 5) k_dispatch_quant_mx(const uint16_t* __restrict__ x, int64_t T, int64_t K,
                                                            int64_t ld, const int32_t* __restrict__ dst_index,
                                                            int top_k, const int32_t* __restrict__ offsets, int32_t G,
                                                            int64_t total, uint8_t* __restrict__ dst_codes,
