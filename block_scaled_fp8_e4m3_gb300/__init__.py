@@ -466,7 +466,8 @@ def sync_install(payload: torch.Tensor, dst: Sequence[SyncEntry], stream=None, c
 def sync_install_noalloc(payload: torch.Tensor, dst: Sequence[SyncEntry], stream=None):
     """sync_install for callers that cannot allocate device memory: the
     library's fixed scratch array is used instead (at most 128 entries;
-    concurrent calls race).  Blocks until the copy is done; a checksum
+    installs are ordered on the device, as for sync_install).  Blocks until
+    the copy is done; a checksum
     mismatch raises FP8Error(FP8_ERR_CHECKSUM)."""
     _check(library().fp8_sync_install_noalloc(payload.data_ptr(), payload.numel(), _entries(dst), len(dst),
                                               _stream(stream)))

@@ -65,6 +65,50 @@ StatusBlock* status_block(fp8_status* err) {
     return g_status[dev];
 }
 
+// Installs share per-device state on the GPU: the status block's checksum
+// accumulator, verdict and grid-barrier counter (fp8_sync_install), or the
+// static scratch (fp8_sync_install_noalloc).  Two installs that overlapped on
+// the device -- issued on different streams or from different host threads --
+// would corrupt each other's verdict, so every install is ordered after the
+// previous one on the device: its stream waits on one event per device, which
+// it then records.  Inside a stream capture the ordering is left to the
+// caller (a capture cannot wait on an event recorded outside it).
+class InstallOrder {
+  public:
+    explicit InstallOrder(cudaStream_t s) : lock_(mu_), s_(s) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaGetDevice(&dev_) != cudaSuccess || dev_ < 0 || dev_ >= kMaxDevices ||
+            cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+            (void)cudaGetLastError();
+            dev_ = -1;
+            return;
+        }
+        if (ev_[dev_] == nullptr && cudaEventCreateWithFlags(&ev_[dev_], cudaEventDisableTiming) != cudaSuccess) {
+            (void)cudaGetLastError();
+            ev_[dev_] = nullptr;
+            dev_ = -1;
+            return;
+        }
+        if (used_[dev_]) err_ = cudaStreamWaitEvent(s, ev_[dev_], 0);
+    }
+    ~InstallOrder() {
+        if (dev_ >= 0 && cudaEventRecord(ev_[dev_], s_) == cudaSuccess) used_[dev_] = true;
+    }
+    cudaError_t error() const { return err_; }
+
+  private:
+    static std::mutex mu_;
+    static cudaEvent_t ev_[kMaxDevices];
+    static bool used_[kMaxDevices];
+    std::lock_guard<std::mutex> lock_;
+    cudaStream_t s_;
+    int dev_ = -1;
+    cudaError_t err_ = cudaSuccess;
+};
+std::mutex InstallOrder::mu_;
+cudaEvent_t InstallOrder::ev_[kMaxDevices] = {};
+bool InstallOrder::used_[kMaxDevices] = {};
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -771,6 +815,8 @@ fp8_status fp8_sync_install(const void* payload_dev, uint64_t bytes, const fp8_s
     StatusBlock* st = status_block(&se);
     if (st == nullptr) return se;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    InstallOrder order(cs);
+    if (order.error() != cudaSuccess) return cuda_fail(order.error(), "sync_install ordering");
     const uint8_t* pay = static_cast<const uint8_t*>(payload_dev);
     std::vector<uint8_t> expect = build_table(dst, n, lay, total);
     std::vector<CopySeg> segs;
@@ -885,6 +931,8 @@ fp8_status fp8_sync_install_noalloc(const void* payload_dev, uint64_t bytes, con
         return fail(FP8_ERR_BAD_PAYLOAD, "payload of %llu bytes, destinations need %llu", (unsigned long long)bytes,
                     (unsigned long long)total);
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    InstallOrder order(cs);
+    if (order.error() != cudaSuccess) return cuda_fail(order.error(), "sync_install_noalloc ordering");
     const uint8_t* pay = static_cast<const uint8_t*>(payload_dev);
 
     // header and table: read back and compare with what dst implies

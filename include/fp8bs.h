@@ -376,7 +376,11 @@ fp8_status fp8_sync_pack(const fp8_sync_entry* entries, int32_t n, void* payload
  * With more entries the header and table are read back and checked on the
  * host (this synchronizes `stream`) and a mismatch is returned at once.  A
  * checksum mismatch writes nothing and fp8_status_poll() returns
- * FP8_ERR_CHECKSUM. */
+ * FP8_ERR_CHECKSUM.  Installs keep their verdict in per-device state, so the
+ * library orders every install after the previous one on the device (its
+ * stream waits on an event the previous install recorded), whatever streams
+ * or host threads issue them; inside a stream capture that ordering is the
+ * caller's. */
 fp8_status fp8_sync_install(const void* payload_dev, uint64_t bytes, const fp8_sync_entry* dst,
                             int32_t n, fp8_stream_t stream);
 
@@ -392,8 +396,10 @@ fp8_status fp8_sync_install(const void* payload_dev, uint64_t bytes, const fp8_s
  * checksum accumulator, the verdict and the segment table, so at most 128
  * entries per call; more returns FP8_ERR_CAPACITY.  The first call on a
  * device looks up the array's device address; make that first call before
- * any stream capture.  Every call shares the array and overwrites it: calls
- * that overlap on the GPU (other streams, other host threads) race.
+ * any stream capture.  Every call shares the array; calls are ordered on
+ * the device as for fp8_sync_install (the same per-device event), so calls
+ * from other streams or host threads do not overlap -- except inside a
+ * stream capture, where the ordering is the caller's.
  * Unlike fp8_sync_install it waits for the copy to finish and reports a
  * checksum mismatch directly (FP8_ERR_CHECKSUM, nothing written); header or
  * table mismatches return FP8_ERR_BAD_PAYLOAD before anything is enqueued.

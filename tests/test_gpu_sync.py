@@ -92,6 +92,39 @@ def test_corrupted_payload_writes_nothing():
     fp8.sync_install(good, dst)
 
 
+def test_installs_on_two_streams_are_ordered():
+    """Installs of a clean and a corrupted payload issued back to back on two
+    streams, ten rounds in both orders: the library orders them on the
+    device, so the clean one lands bit for bit, the corrupted one writes
+    nothing, and the checksum verdicts do not mix."""
+    W, X, M, N = _trainer_tensors(seed=30)
+    entries = _entries(W, X, M, N)
+    good = fp8.sync_pack(entries)
+    bad = good.clone()
+    bad[bad.numel() // 2] ^= 0x40
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for r in range(10):
+        d_good, d_bad = _empty_like(entries), _empty_like(entries)
+        torch.cuda.synchronize()
+        order = [(s1, good, d_good), (s2, bad, d_bad)]
+        for s, payload, dst in (order if r % 2 == 0 else order[::-1]):
+            fp8.sync_install(payload, dst, stream=s, check=False)
+        torch.cuda.synchronize()
+        with pytest.raises(fp8.FP8Error) as ei:
+            fp8.status_poll()
+        assert ei.value.status == 5                           # FP8_ERR_CHECKSUM, from the corrupted one
+        for src, d in zip(entries, d_good):
+            a, b = (src.tensor, d.tensor)
+            if isinstance(a, fp8.QTensor):
+                assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+            else:
+                assert torch.equal(a, b)
+        for d in d_bad:
+            t = d.tensor.codes if isinstance(d.tensor, fp8.QTensor) else d.tensor
+            assert int(t.view(torch.uint8).count_nonzero()) == 0
+    fp8.status_poll()
+
+
 def test_header_mismatch_rejected():
     W, X, M, N = _trainer_tensors(seed=20)
     entries = _entries(W, X, M, N)
