@@ -233,8 +233,8 @@ def breakdown(fp8, synth, dev, flush, pk, reps):
         out[name] = d
 
     # tiny blockwise configuration (X 128x512, W 512x512): launch-latency bound,
-    # reported without a roofline; the quantize + GEMM part also as one CUDA
-    # graph replay (the sync calls copy a host header, so they stay eager)
+    # reported without a roofline; eager, and replayed as one CUDA graph (the
+    # quantize + GEMM part, and the whole step with pack and install)
     wl = synth.tiny()
     Xt, Wt = wl.tensors["X"].to(dev), wl.tensors["W"].to(dev)
     qxt, qwt = fp8.quantize_group(Xt, "K"), fp8.quantize_block(Wt)
@@ -272,6 +272,16 @@ def breakdown(fp8, synth, dev, flush, pk, reps):
         del graph
     except Exception as e:  # noqa: BLE001 - reported, the rest of the breakdown still runs
         out["tiny_quant_gemm_graph"] = {"error": str(e).splitlines()[0][:200]}
+    try:
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            tiny_step()
+        out["tiny_step_graph"] = {"ms": round(time_kernel(graph.replay, flush, reps), 5), "bound": "launch",
+                                  "workload": "the five-kernel step (with pack and install) replayed as one CUDA graph"}
+        del graph
+    except Exception as e:  # noqa: BLE001
+        out["tiny_step_graph"] = {"error": str(e).splitlines()[0][:200]}
     del Xt, Wt, qxt, qwt, Yt, pt, rt
 
     # dense MLP forward + sync

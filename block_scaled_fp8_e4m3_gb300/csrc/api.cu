@@ -775,9 +775,25 @@ fp8_status fp8_sync_pack(const fp8_sync_entry* entries, int32_t n, void* payload
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* pay = static_cast<uint8_t*>(payload_dev);
     std::vector<uint8_t> h = build_table(entries, n, lay, total);
-    put64(&h[32], table_checksum(h));  // the segment words are added on the device
-    cudaError_t e = cudaMemcpyAsync(pay, h.data(), h.size(), cudaMemcpyHostToDevice, cs);
-    if (e != cudaSuccess) return cuda_fail(e, "sync_pack header copy");
+    const unsigned long long tsum = table_checksum(h);   // the segment words are added on the device
+    // A header and table that fit a kernel parameter are written by the pack
+    // kernel itself (after the checksum field is zeroed), so the call is pure
+    // device work: no host staging and nothing that keeps it out of a CUDA
+    // graph.  Larger ones are copied from the host.
+    static thread_local ExpectTable hdr;
+    const ExpectTable* hdr_ptr = nullptr;
+    cudaError_t e;
+    if (h.size() <= (size_t)kMaxExpectBytes) {
+        hdr.bytes = (uint32_t)h.size();
+        memcpy(hdr.data, h.data(), h.size());
+        hdr_ptr = &hdr;
+        e = cudaMemsetAsync(pay + 32, 0, 8, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "sync_pack checksum field");
+    } else {
+        put64(&h[32], tsum);
+        e = cudaMemcpyAsync(pay, h.data(), h.size(), cudaMemcpyHostToDevice, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "sync_pack header copy");
+    }
     // segments: each covers the bytes up to the next segment start
     std::vector<CopySeg> segs;
     for (int32_t i = 0; i < n; ++i) {
@@ -792,9 +808,9 @@ fp8_status fp8_sync_pack(const fp8_sync_entry* entries, int32_t n, void* payload
         }
     }
     unsigned long long* csum = reinterpret_cast<unsigned long long*>(pay + 32);
-    for (size_t b = 0; b < segs.size(); b += kMaxCopySegs) {
+    for (size_t b = 0; b < segs.size() || (b == 0 && hdr_ptr != nullptr); b += kMaxCopySegs) {
         const int cnt = (int)std::min<size_t>(kMaxCopySegs, segs.size() - b);
-        e = launch_sync_pack(&segs[b], cnt, csum, cs);
+        e = launch_sync_pack(segs.data() + b, cnt, csum, b == 0 ? hdr_ptr : nullptr, tsum, cs);
         if (e != cudaSuccess) return cuda_fail(e, "sync_pack");
     }
     if (used_bytes) *used_bytes = total;

@@ -90,14 +90,19 @@ struct CopySeg {
     uint64_t padded;  // bytes written at dst (zero fill after `bytes`); multiple of 16
     uint64_t dst_word0;  // payload word index of dst[0] (pack: checksum position)
 };
-cudaError_t launch_sync_pack(const CopySeg* segs, int n, unsigned long long* checksum_field, cudaStream_t st);
-// Expected header + entry table of a payload, compared on the device with
-// the payload's own bytes (the checksum field excepted); bytes == 0: none.
+// Header + entry table of a payload (the checksum field excepted): written
+// by the pack kernel, or compared on the device with the payload's own bytes
+// by the install kernels; bytes == 0: none.
 constexpr int kMaxExpectBytes = 64 + 128 * 24;
 struct ExpectTable {
     uint32_t bytes;
     uint8_t data[kMaxExpectBytes];
 };
+// Pack: segment copies with the checksum accumulated into *checksum_field;
+// with hdr, the first launch also writes the header and table and adds
+// table_sum (the caller zeroes the checksum field first).
+cudaError_t launch_sync_pack(const CopySeg* segs, int n, unsigned long long* checksum_field, const ExpectTable* hdr,
+                             unsigned long long table_sum, cudaStream_t st);
 // Verify + scatter in one cooperative launch; cudaErrorNotSupported when
 // the device cannot run it (or n > kMaxCopySegs): use the two kernels then.
 cudaError_t launch_sync_install(const uint8_t* payload, uint64_t data_offset, uint64_t total_bytes,

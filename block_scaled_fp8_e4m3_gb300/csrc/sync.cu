@@ -68,8 +68,19 @@ __device__ __forceinline__ unsigned long long block_sum(unsigned long long v) {
 
 constexpr int kUnroll = 4;
 
-__global__ void __launch_bounds__(256) k_sync_pack(const SegTable tab, unsigned long long* checksum_field) {
+// hdr.bytes != 0: block 0 also writes the payload's header and entry table
+// (every byte but the checksum field, which the caller zeroed) and adds the
+// table's share of the checksum, so the whole pack is device work.
+__global__ void __launch_bounds__(256) k_sync_pack(const SegTable tab, unsigned long long* checksum_field,
+                                                   const __grid_constant__ ExpectTable hdr,
+                                                   unsigned long long table_sum) {
     __shared__ uint64_t start[kMaxCopySegs + 1];
+    if (blockIdx.x == 0 && hdr.bytes != 0) {
+        uint8_t* head = reinterpret_cast<uint8_t*>(checksum_field) - 32;
+        for (uint32_t i = threadIdx.x; i < hdr.bytes; i += blockDim.x)
+            if (i < 32 || i >= 40) head[i] = hdr.data[i];
+        if (threadIdx.x == 0) atomicAdd(checksum_field, table_sum);
+    }
     if (threadIdx.x == 0) {
         uint64_t acc = 0;
         for (int s = 0; s < tab.n; ++s) {
@@ -320,7 +331,9 @@ cudaError_t launch_wait_expiry(unsigned long long limit_ns, StatusBlock* status,
     return cudaGetLastError();
 }
 
-cudaError_t launch_sync_pack(const CopySeg* segs, int n, unsigned long long* checksum_field, cudaStream_t st) {
+cudaError_t launch_sync_pack(const CopySeg* segs, int n, unsigned long long* checksum_field, const ExpectTable* hdr,
+                             unsigned long long table_sum, cudaStream_t st) {
+    static const ExpectTable none = {};
     SegTable tab;
     uint64_t chunks = 0;
     tab.n = n;
@@ -328,8 +341,9 @@ cudaError_t launch_sync_pack(const CopySeg* segs, int n, unsigned long long* che
         tab.seg[i] = segs[i];
         chunks += segs[i].padded / 16;
     }
-    if (chunks == 0) return cudaSuccess;
-    k_sync_pack<<<grid_for(k_sync_pack, chunks), 256, 0, st>>>(tab, checksum_field);
+    if (chunks == 0 && hdr == nullptr) return cudaSuccess;
+    const unsigned grid = chunks == 0 ? 1u : grid_for(k_sync_pack, chunks);
+    k_sync_pack<<<grid, 256, 0, st>>>(tab, checksum_field, hdr ? *hdr : none, table_sum);
     return cudaGetLastError();
 }
 

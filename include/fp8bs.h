@@ -361,8 +361,11 @@ fp8_status fp8_sync_payload_size(const fp8_sync_entry* entries, int32_t n, uint6
 
 /* Packs the entries (device tensors) into payload_dev (device, capacity
  * bytes, 256-byte aligned).  *used_bytes (host) receives the payload size.
- * The header/table are copied from the host; the segment copy and the
- * checksum run on the device. */
+ * The segment copy and the checksum run on the device.  When the header and
+ * table fit 3136 bytes (up to 23 entries) the pack kernel writes them too,
+ * so the call is device work only and can be captured in a CUDA graph;
+ * larger tables are copied from the host (a pageable copy, which waits for
+ * the stream). */
 fp8_status fp8_sync_pack(const fp8_sync_entry* entries, int32_t n, void* payload_dev,
                          uint64_t capacity, uint64_t* used_bytes, fp8_stream_t stream);
 
@@ -370,7 +373,7 @@ fp8_status fp8_sync_pack(const fp8_sync_entry* entries, int32_t n, void* payload
  * buffers of the rollout side).  Never quantizes: the bytes are copied.
  * Every header and table byte (the checksum field excepted) must equal what
  * dst implies, and the checksum must match; both are verified on the device
- * before any destination byte is written.  For up to 24 entries the header
+ * before any destination byte is written.  For up to 23 entries the header
  * check also runs on the device (the call does not synchronize `stream`): a
  * mismatch writes nothing and fp8_status_poll() returns FP8_ERR_BAD_PAYLOAD.
  * With more entries the header and table are read back and checked on the

@@ -158,7 +158,7 @@ def test_full_mlp_weight_round_trip():
 
 def test_many_entries_use_the_two_kernel_path():
     """30 quantized entries (60 segments, more than one cooperative launch's
-    table of 32, and more than the 24 entries whose header the device checks):
+    table of 32, and more than the 23 entries whose header the device checks):
     the verify + scatter path and the host header check.  The payload equals
     the oracle's, the round trip is bit-identical, and a corrupted payload
     writes nothing."""
