@@ -223,3 +223,30 @@ def test_zero_rows_and_mismatched_operands():
     assert err.value.status == 3
     fp8.status_poll()
     torch.testing.assert_close(fp8.gemm(qx, qw), fp8.gemm(qx, qw))    # still usable afterwards
+
+
+@pytest.mark.parametrize("recipe", ["blockwise", "pow2", "mx"])
+def test_strided_output(recipe):
+    """D written into a view with a row pitch above N (912 bytes: 16-byte but
+    not 32-byte aligned rows, so the 16-byte store path runs): the same
+    values as a contiguous D, the fused quantization unchanged, and the
+    padding columns untouched."""
+    M, N, K = 300, 384, 512
+    X, W = _fwd_case(M, N, K, seed=77)
+    if recipe == "mx":
+        qa, qb = fp8.quantize_mx(X.to(DEV)), fp8.quantize_mx(W.to(DEV))
+    else:
+        p2 = recipe == "pow2"
+        qa, qb = fp8.quantize_group(X.to(DEV), "K", pow2=p2), fp8.quantize_block(W.to(DEV), pow2=p2)
+    Y, qy = fp8.gemm(qa, qb, quantize_output=True)
+    buf = torch.full((M, N + 72), 7.0, dtype=torch.bfloat16, device=DEV)
+    Yv, qv = fp8.gemm(qa, qb, out=buf[:, :N], quantize_output=True)
+    assert Yv.stride(0) == N + 72
+    assert torch.equal(Yv, Y)
+    assert torch.equal(qv.codes, qy.codes) and torch.equal(qv.scales, qy.scales)
+    assert bool((buf[:, N:] == 7.0).all())
+    if recipe == "blockwise":
+        Yf = fp8.gemm(qa, qb, out_dtype=torch.float32)
+        fbuf = torch.full((M, N + 40), 7.0, dtype=torch.float32, device=DEV)
+        Yfv = fp8.gemm(qa, qb, out=fbuf[:, :N])
+        assert torch.equal(Yfv, Yf) and bool((fbuf[:, N:] == 7.0).all())
