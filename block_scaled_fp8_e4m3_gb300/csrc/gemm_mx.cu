@@ -164,14 +164,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) tmem_alloc_pair(&bar->tmem_base, kMxTmemCols);
     if (warp == 2) {
-        // group row offsets and the prefix sums of their 128- and 256-row tile counts
+        // group row offsets and the prefix sums of their 128- and 256-row tile
+        // counts.  Offsets outside [0, M] or decreasing are reported
+        // (FP8_ERR_INVALID_ARG at the next status poll) and clamped to [0, M],
+        // so every row the kernel touches stays inside A and D.
         int carry = 0, carry2 = 0;
+        bool bad = false;
         for (int base = 0; base < G; base += 32) {
             const int g = base + lane;
             int o0 = 0, o1 = 0;
             if (g < G) {
                 o0 = p.m_offsets ? p.m_offsets[g] : 0;
                 o1 = p.m_offsets ? p.m_offsets[g + 1] : p.M;
+                bad |= o0 < 0 || o1 < o0 || o1 > p.M || (g == 0 && o0 != 0);
+                o0 = o0 < 0 ? 0 : (o0 > p.M ? p.M : o0);
+                o1 = o1 < o0 ? o0 : (o1 > p.M ? p.M : o1);
                 offs[g] = o0;
             }
             int cnt = (g < G) ? (o1 - o0 + BM - 1) / BM : 0;
@@ -197,9 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             pfx[G] = carry;
             pfx2[G] = carry2;
-            offs[G] = p.m_offsets ? p.m_offsets[G] : p.M;
+            const int oG = p.m_offsets ? p.m_offsets[G] : p.M;
+            offs[G] = oG < 0 ? 0 : (oG > p.M ? p.M : oG);
             bar->num_mtiles = carry2;
         }
+        if (__any_sync(0xffffffffu, bad) && lane == 0 && rank == 0) atomicOr(&p.st->error_bits, kErrDeviceArg);
     }
     tc_fence_before();
     cluster_sync();  // barriers, group tables and TMEM ready in both CTAs

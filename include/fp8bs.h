@@ -328,7 +328,11 @@ fp8_status fp8_gemm_blockscaled(const fp8_tensor* A, const fp8_tensor* B, void* 
  *    MX_1x32_GROUPED (from fp8_permute_rows_mx).
  * B_stack: MXFP8 rows = num_groups * N, layout MX_1x32 (fp8_quantize_mx of
  *    the [num_groups*N][K] weight stack).
- * m_offsets_dev: int32 [num_groups+1] on the device (see above).
+ * m_offsets_dev: int32 [num_groups+1] on the device (see above).  The
+ *    kernel checks them: offsets that are negative, decreasing, above
+ *    total_rows, or that do not start at 0 are clamped to [0, total_rows]
+ *    (no row outside A or D is touched) and fp8_status_poll() returns
+ *    FP8_ERR_INVALID_ARG.
  * D: bf16 [total_rows][ldd].  Requires K % 128 == 0, N % 256 == 0,
  * 1 <= num_groups <= 1024. */
 fp8_status fp8_grouped_gemm(const fp8_tensor* A, const fp8_tensor* B_stack,

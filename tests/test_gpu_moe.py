@@ -94,6 +94,29 @@ def test_moe_empty_and_single_row_groups():
             assert_gemm_close(Y[a:b].double().cpu().numpy(), ref, mag, f"group {g}")
 
 
+@pytest.mark.parametrize("bad", [[0, 100, 450, 300], [0, 150, 100, 300], [-5, 100, 200, 300], [0, 100, 200, 340]])
+def test_bad_group_offsets_are_reported_and_contained(bad):
+    """Group offsets past the rows of A, decreasing, or negative: the grouped
+    GEMM reports FP8_ERR_INVALID_ARG at the next status poll, writes nothing
+    outside D's rows, and later calls with valid offsets are exact again."""
+    K, N, G = 256, 256, 3
+    offsets = torch.tensor([0, 100, 200, 300], dtype=torch.int32)
+    X = synth.random_bf16((300, K), seed=21, outliers=True)
+    gather = torch.arange(300, dtype=torch.int32)
+    W = synth.random_bf16((G, N, K), seed=22, std=0.02)
+    qa, Y = _run(X, W, gather, offsets)
+    qw = fp8.quantize_mx(W.reshape(G * N, K).to(DEV))
+    buf = torch.full((300 + 64, N), 7.0, dtype=torch.bfloat16, device=DEV)
+    fp8.grouped_gemm(qa, qw, torch.tensor(bad, dtype=torch.int32, device=DEV), N, out=buf[:300])
+    with pytest.raises(fp8.FP8Error) as ei:
+        fp8.status_poll()
+    assert ei.value.status == 1
+    assert bool((buf[300:] == 7.0).all())
+    Y2 = fp8.grouped_gemm(qa, qw, offsets.to(DEV), N)
+    fp8.status_poll()
+    assert torch.equal(Y2, Y)
+
+
 def test_full_moe_sampled():
     X, W, gather, offsets = _moe_case(16384, 64, 8, 2048, 1024, 4)
     qa, Y = _run(X, W, gather, offsets)
