@@ -641,11 +641,24 @@ __global__ void __launch_bounds__(256) k_permute_rows_mx(const uint8_t* __restri
         if (offsets[mid] <= i) lo = mid; else hi = mid;
     }
     const int g = lo;
-    // atom-row base of group g: sum over h < g of ceil(M_h / 128)
+    // atom-row base of group g: sum over h < g of ceil(M_h / 128).  The
+    // offsets are checked on the way (offsets[0] = 0, non-decreasing up to
+    // g, offsets[g] <= i < offsets[g + 1]): otherwise the row is reported and
+    // not written, so no scale word lands outside the grouped layout.
     int64_t pg = 0;
-    for (int h = lane; h < g; h += 32) pg += (offsets[h + 1] - offsets[h] + 127) / 128;
+    bool ok = true;
+    for (int h = lane; h < g; h += 32) {
+        const int32_t a = offsets[h], b = offsets[h + 1];
+        ok &= b >= a;
+        pg += (b - a + 127) / 128;
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) pg += __shfl_xor_sync(0xffffffffu, pg, o);
+    ok = __all_sync(0xffffffffu, ok) && offsets[0] == 0 && offsets[g] <= i && i < offsets[g + 1];
+    if (!ok) {
+        if (lane == 0) atomicOr(&status->error_bits, kErrDeviceArg);
+        return;
+    }
     const int64_t l = i - offsets[g];
 
     const uint4* s4 = reinterpret_cast<const uint4*>(src_codes + src * K);
@@ -682,17 +695,25 @@ __global__ void __launch_bounds__(256, 5) k_dispatch_quant_mx(const uint16_t* __
                                                            uint8_t* __restrict__ dst_scales, StatusBlock* status) {
     __shared__ int32_t s_off[kDqMaxGroups + 1];
     __shared__ int64_t s_pg[kDqMaxGroups + 1];
+    __shared__ int s_bad;
     for (int g = threadIdx.x; g <= G; g += blockDim.x) s_off[g] = offsets[g];
     __syncthreads();
     if (threadIdx.x == 0) {
+        // offsets must run from 0 to total without decreasing; otherwise the
+        // call is reported and nothing is written
+        int bad = s_off[0] != 0 || s_off[G] != total;
         int64_t acc = 0;
         for (int g = 0; g < G; ++g) {
             s_pg[g] = acc;
+            bad |= s_off[g + 1] < s_off[g];
             acc += (s_off[g + 1] - s_off[g] + 127) / 128;
         }
         s_pg[G] = acc;
+        s_bad = bad;
+        if (bad) atomicOr(&status->error_bits, kErrDeviceArg);
     }
     __syncthreads();
+    if (s_bad) return;
     const int lane = threadIdx.x & 31, sub = lane & 15, half = lane >> 4;
     const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;

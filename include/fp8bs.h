@@ -263,8 +263,10 @@ int64_t fp8_mx_grouped_scale_bytes(int64_t total_rows, int64_t cols, int32_t num
  * device, non-decreasing, m_offsets[0] = 0, m_offsets[num_groups] =
  * total_rows.  src: MXFP8, layout MX_1x32; dst: rows = total_rows, same cols,
  * layout MX_1x32_GROUPED with fp8_mx_grouped_scale_bytes() bytes of scales.
- * Requires cols % 128 == 0.  Out-of-range gather entries are skipped on the
- * device and reported as FP8_ERR_INVALID_ARG by fp8_status_poll(). */
+ * Requires cols % 128 == 0.  Out-of-range gather entries, and rows whose
+ * group offsets break the rules above, are skipped on the device and
+ * reported as FP8_ERR_INVALID_ARG by fp8_status_poll(); nothing is written
+ * outside dst. */
 fp8_status fp8_permute_rows_mx(const fp8_tensor* src, const int32_t* gather_dev,
                                const int32_t* m_offsets_dev, int32_t num_groups,
                                const fp8_tensor* dst, fp8_stream_t stream);
@@ -282,7 +284,9 @@ fp8_status fp8_permute_rows_mx(const fp8_tensor* src, const int32_t* gather_dev,
  *                 their codes, their scales read 0).
  *  m_offsets_dev, num_groups, dst: as for fp8_permute_rows_mx (dst->cols = K).
  * Requires K % 128 == 0, 0 <= top_k <= 64.  Out-of-range entries are skipped
- * on the device and reported as FP8_ERR_INVALID_ARG by fp8_status_poll(). */
+ * on the device and reported as FP8_ERR_INVALID_ARG by fp8_status_poll();
+ * group offsets that break the rules of fp8_permute_rows_mx are reported
+ * the same way and no codes are written (the scales read 0). */
 fp8_status fp8_dispatch_quantize_mx(const void* x_bf16, int64_t T, int64_t K, int64_t ld, const int32_t* dst_index_dev,
                                     int32_t top_k, const int32_t* m_offsets_dev, int32_t num_groups,
                                     const fp8_tensor* dst, fp8_stream_t stream);

@@ -117,6 +117,35 @@ def test_bad_group_offsets_are_reported_and_contained(bad):
     assert torch.equal(Y2, Y)
 
 
+@pytest.mark.parametrize("bad", [[0, 150, 100, 300], [10, 100, 200, 300], [0, 100, 200, 290], [-128, 100, 200, 300]])
+def test_permute_and_dispatch_reject_bad_offsets(bad):
+    """Group offsets that decrease, do not start at 0 or do not end at the
+    row count: the row gather and the fused dispatch report
+    FP8_ERR_INVALID_ARG and write nothing outside the destination buffers
+    (the dispatch writes no codes at all)."""
+    rows, K, G = 300, 256, 3
+    X = synth.random_bf16((rows, K), seed=31, outliers=True).to(DEV)
+    qx = fp8.quantize_mx(X)
+    sb = fp8.mx_grouped_scale_bytes(rows, K, G)
+    codes_buf = torch.full((rows + 8, K), 0x5A, dtype=torch.uint8, device=DEV)
+    scales_buf = torch.full((sb + 4096,), 0x5A, dtype=torch.uint8, device=DEV)
+    out = fp8.QTensor(codes_buf[:rows], scales_buf[:sb], rows, K, fp8.RECIPE_MX, fp8.LAYOUT_MX_1x32_GROUPED)
+    off = torch.tensor(bad, dtype=torch.int32, device=DEV)
+    fp8.permute_rows_mx(qx, torch.arange(rows, dtype=torch.int32, device=DEV), off, out=out)
+    with pytest.raises(fp8.FP8Error) as ei:
+        fp8.status_poll()
+    assert ei.value.status == 1
+    assert bool((codes_buf[rows:] == 0x5A).all()) and bool((scales_buf[sb:] == 0x5A).all())
+    codes_buf.fill_(0x5A)
+    scales_buf.fill_(0x5A)
+    dst_index = torch.arange(rows, dtype=torch.int32, device=DEV).reshape(rows, 1)
+    fp8.dispatch_quantize_mx(X, dst_index, off, rows, out=out)
+    with pytest.raises(fp8.FP8Error) as ei:
+        fp8.status_poll()
+    assert ei.value.status == 1
+    assert bool((codes_buf == 0x5A).all()) and bool((scales_buf[sb:] == 0x5A).all())
+
+
 def test_full_moe_sampled():
     X, W, gather, offsets = _moe_case(16384, 64, 8, 2048, 1024, 4)
     qa, Y = _run(X, W, gather, offsets)
