@@ -641,10 +641,16 @@ __global__ void __launch_bounds__(256) k_permute_rows_mx(const uint8_t* __restri
         if (offsets[mid] <= i) lo = mid; else hi = mid;
     }
     const int g = lo;
+    // the codes row lies inside dst whatever the offsets say
+    const uint4* s4 = reinterpret_cast<const uint4*>(src_codes + src * K);
+    uint4* d4 = reinterpret_cast<uint4*>(dst_codes + i * K);
+    for (int64_t c = lane; c < K / 16; c += 32) d4[c] = s4[c];
+
     // atom-row base of group g: sum over h < g of ceil(M_h / 128).  The
     // offsets are checked on the way (offsets[0] = 0, non-decreasing up to
-    // g, offsets[g] <= i < offsets[g + 1]): otherwise the row is reported and
-    // not written, so no scale word lands outside the grouped layout.
+    // g, offsets[g] <= i < offsets[g + 1]): otherwise the row's scale words
+    // are not written and the call is reported, so none lands outside the
+    // grouped layout.
     int64_t pg = 0;
     bool ok = true;
     for (int h = lane; h < g; h += 32) {
@@ -660,10 +666,6 @@ __global__ void __launch_bounds__(256) k_permute_rows_mx(const uint8_t* __restri
         return;
     }
     const int64_t l = i - offsets[g];
-
-    const uint4* s4 = reinterpret_cast<const uint4*>(src_codes + src * K);
-    uint4* d4 = reinterpret_cast<uint4*>(dst_codes + i * K);
-    for (int64_t c = lane; c < K / 16; c += 32) d4[c] = s4[c];
 
     const int64_t atoms_k = K / 128;
     const int64_t s_in = (src & 31) * 16 + ((src & 127) >> 5) * 4;

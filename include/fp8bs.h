@@ -263,10 +263,10 @@ int64_t fp8_mx_grouped_scale_bytes(int64_t total_rows, int64_t cols, int32_t num
  * device, non-decreasing, m_offsets[0] = 0, m_offsets[num_groups] =
  * total_rows.  src: MXFP8, layout MX_1x32; dst: rows = total_rows, same cols,
  * layout MX_1x32_GROUPED with fp8_mx_grouped_scale_bytes() bytes of scales.
- * Requires cols % 128 == 0.  Out-of-range gather entries, and rows whose
- * group offsets break the rules above, are skipped on the device and
- * reported as FP8_ERR_INVALID_ARG by fp8_status_poll(); nothing is written
- * outside dst. */
+ * Requires cols % 128 == 0.  Out-of-range gather entries are skipped on the
+ * device; rows whose group offsets break the rules above get their codes
+ * but no scale words.  Both are reported as FP8_ERR_INVALID_ARG by
+ * fp8_status_poll(), and nothing is written outside dst. */
 fp8_status fp8_permute_rows_mx(const fp8_tensor* src, const int32_t* gather_dev,
                                const int32_t* m_offsets_dev, int32_t num_groups,
                                const fp8_tensor* dst, fp8_stream_t stream);
