@@ -60,3 +60,36 @@ def oracle_block(w: torch.Tensor, transposed=False):
 
 def oracle_mx(x: torch.Tensor):
     return oracle.quant_mx_1x32(synth.bf16_bits(x))
+
+
+def stratified_positions(M: int, N: int, per_tile: int = 16, tile: int = 256, seed: int = 0,
+                         row_segments=None):
+    """Output positions for a sampled GEMM check: every tile x tile block of
+    the output (tiles start at each row segment's first row when
+    row_segments = [(start, end), ...] is given, as the grouped GEMM tiles
+    each expert's rows) contributes its four corners and per_tile - 4
+    uniform positions.  A wrong tile cannot escape the check."""
+    rng = np.random.default_rng(seed)
+    segs = row_segments if row_segments is not None else [(0, M)]
+    ms, ns = [], []
+    extra = max(per_tile - 4, 0)
+    for s0, s1 in segs:
+        for t0 in range(s0, s1, tile):
+            t1 = min(s1, t0 + tile)
+            for u0 in range(0, N, tile):
+                u1 = min(N, u0 + tile)
+                ms.extend([t0, t0, t1 - 1, t1 - 1])
+                ns.extend([u0, u1 - 1, u0, u1 - 1])
+                ms.extend(rng.integers(t0, t1, extra).tolist())
+                ns.extend(rng.integers(u0, u1, extra).tolist())
+    return np.asarray(ms, np.int64), np.asarray(ns, np.int64)
+
+
+def sampled_gemm_check(Y: torch.Tensor, A_deq, B_deq, what: str, seed: int = 0, per_tile: int = 16):
+    """Y = A B^T checked at stratified positions against the oracle's fp64
+    reference of those outputs."""
+    M, N = Y.shape
+    ms, ns = stratified_positions(M, N, per_tile=per_tile, seed=seed)
+    ref, mag = oracle.gemm_ref_sampled(A_deq, B_deq, ms, ns)
+    got = Y[torch.from_numpy(ms).to(Y.device), torch.from_numpy(ns).to(Y.device)].double().cpu().numpy()
+    assert_gemm_close(got, ref, mag, what)

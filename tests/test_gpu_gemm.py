@@ -10,7 +10,7 @@ import block_scaled_fp8_e4m3_gb300 as fp8
 import oracle
 from block_scaled_fp8_e4m3_gb300 import synth
 from gpu_util import (DEV, assert_bytes_equal, assert_gemm_close, bf16_dev_to_f64, oracle_block, oracle_group_k,
-                      oracle_group_m, oracle_mx, to_np)
+                      oracle_group_m, oracle_mx, sampled_gemm_check, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -102,6 +102,42 @@ def test_mx_fused_quant():
     q2 = fp8.quantize_mx(Y)
     assert_bytes_equal(to_np(qy.codes), to_np(q2.codes), "fused codes")
     assert_bytes_equal(to_np(qy.scales), to_np(q2.scales), "fused scales")
+    # and the oracle's MX 1x32 quantization of the returned bf16 Y
+    c, s = oracle_mx(Y.cpu())
+    assert_bytes_equal(to_np(qy.codes), c, "fused codes vs oracle")
+    assert_bytes_equal(to_np(qy.scales), s, "fused scales vs oracle")
+
+
+def _mx_row_scales(scales: np.ndarray, rows, K: int) -> np.ndarray:
+    """E8M0 bytes [len(rows), K/32] of the given rows, read out of the MX
+    scale-factor atom layout of a [R, K] tensor."""
+    out = np.empty((len(rows), K // 32), np.uint8)
+    for i, r in enumerate(rows):
+        for j in range(K // 32):
+            out[i, j] = scales[oracle.mx_scale_offset(int(r), j, K)]
+    return out
+
+
+@pytest.mark.parametrize("recipe", ["blockwise", "mx"])
+def test_multi_tile_elementwise(recipe):
+    """Every output of a GEMM large enough that each CTA pair of the
+    persistent grid computes at least three 256x256 tiles (4096x4096: 256
+    tiles on at most 76 pairs), against the oracle element by element: the
+    TMEM set alternation and barrier phases across tiles are all checked."""
+    M, N, K = 4096, 4096, 384 if recipe == "blockwise" else 256
+    X, W = _fwd_case(M, N, K, seed=4096 + K)
+    if recipe == "blockwise":
+        Y = fp8.gemm(fp8.quantize_group(X.to(DEV), "K"), fp8.quantize_block(W.to(DEV)))
+        cx, sx = oracle_group_k(X)
+        cw, sw = oracle_block(W)
+        a, b = oracle.dequant_group(cx, sx), oracle.dequant_block(cw, sw)
+    else:
+        Y = fp8.gemm(fp8.quantize_mx(X.to(DEV)), fp8.quantize_mx(W.to(DEV)))
+        cx, sx = oracle_mx(X)
+        cw, sw = oracle_mx(W)
+        a, b = oracle.dequant_mx(cx, sx), oracle.dequant_mx(cw, sw)
+    ref, mag = oracle.gemm_ref(a, b)
+    assert_gemm_close(bf16_dev_to_f64(Y), ref, mag, f"{recipe} {M}x{N}x{K} all outputs")
 
 
 def test_mx_scale_factors_are_applied_per_row_and_block():
@@ -139,17 +175,10 @@ def test_blockwise_scales_closed_form():
 
 
 # ---------------------------------------------------------------- full size, sampled
-def _sampled_check(Y, A_deq, B_deq, what, n=4096, seed=0):
-    rng = np.random.default_rng(seed)
-    M, N = Y.shape
-    ms = rng.integers(0, M, n)
-    ns = rng.integers(0, N, n)
-    # always include the corners and tile edges
-    ms = np.concatenate([ms, [0, M - 1, 127, 128, M - 1]])
-    ns = np.concatenate([ns, [0, N - 1, 255, 256, 0]])
-    ref, mag = oracle.gemm_ref_sampled(A_deq, B_deq, ms, ns)
-    got = Y[torch.from_numpy(ms).to(Y.device), torch.from_numpy(ns).to(Y.device)].double().cpu().numpy()
-    assert_gemm_close(got, ref, mag, what)
+def _sampled_check(Y, A_deq, B_deq, what, seed=0):
+    """Stratified: the four corners and 12 uniform positions of every 256x256
+    output tile (the kernels' tile), against the oracle."""
+    sampled_gemm_check(Y, A_deq, B_deq, what, seed=seed)
 
 
 def test_full_mlp_forward_sampled():
@@ -190,10 +219,19 @@ def test_full_backward_sampled():
 def test_full_mx_sampled():
     wl = synth.mx()
     X, W = wl.tensors["X"], wl.tensors["W"]
-    Y = fp8.gemm(fp8.quantize_mx(X.to(DEV)), fp8.quantize_mx(W.to(DEV)))
+    Y, qy = fp8.gemm(fp8.quantize_mx(X.to(DEV)), fp8.quantize_mx(W.to(DEV)), quantize_output=True)
     cx, sx = oracle_mx(X)
     cw, sw = oracle_mx(W)
     _sampled_check(Y, oracle.dequant_mx(cx, sx), oracle.dequant_mx(cw, sw), "mx full")
+    # the fused MX quantization of Y against the oracle, on sampled rows
+    # (including the first and last row of the 128-row scale atoms)
+    N = Y.shape[1]
+    rows = np.unique(np.concatenate([np.random.default_rng(5).choice(Y.shape[0], 64, replace=False),
+                                     [0, 127, 128, Y.shape[0] - 1]]))
+    c, s = oracle_mx(Y[torch.from_numpy(rows).to(Y.device)].cpu())
+    assert_bytes_equal(to_np(qy.codes)[rows], c, "fused MX codes, sampled rows")
+    assert_bytes_equal(_mx_row_scales(to_np(qy.scales), rows, N), _mx_row_scales(s, range(len(rows)), N),
+                       "fused MX scales, sampled rows")
 
 
 def test_zero_rows_and_mismatched_operands():

@@ -8,7 +8,7 @@ import torch
 import block_scaled_fp8_e4m3_gb300 as fp8
 import oracle
 from block_scaled_fp8_e4m3_gb300 import synth
-from gpu_util import DEV, assert_bytes_equal, assert_gemm_close, oracle_mx, to_np
+from gpu_util import DEV, assert_bytes_equal, assert_gemm_close, oracle_mx, stratified_positions, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -156,9 +156,10 @@ def test_full_moe_sampled():
     cw, sw = oracle_mx(W.reshape(G * N, K))
     A_deq_src = oracle.dequant_mx(cx, sx)
     W_deq = oracle.dequant_mx(cw, sw)
-    rng = np.random.default_rng(1)
-    rows = rng.integers(0, off_np[-1], 4096)
-    cols = rng.integers(0, N, 4096)
+    # stratified over the kernel's tiles: 256-row tiles from each expert's
+    # first row, 256-column tiles
+    segs = [(int(off_np[e]), int(off_np[e + 1])) for e in range(G) if off_np[e + 1] > off_np[e]]
+    rows, cols = stratified_positions(int(off_np[-1]), N, seed=1, row_segments=segs)
     grp = np.searchsorted(off_np, rows, side="right") - 1
     ref, mag = oracle.gemm_ref_sampled(A_deq_src, W_deq, g_np[rows].astype(np.int64), grp * N + cols)
     got = Y[torch.from_numpy(rows).to(DEV), torch.from_numpy(cols).to(DEV)].double().cpu().numpy()

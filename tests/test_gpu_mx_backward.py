@@ -8,7 +8,7 @@ import pytest
 import block_scaled_fp8_e4m3_gb300 as fp8
 import oracle
 from block_scaled_fp8_e4m3_gb300 import synth
-from gpu_util import DEV, assert_bytes_equal, assert_gemm_close, bf16_dev_to_f64, to_np
+from gpu_util import DEV, assert_bytes_equal, assert_gemm_close, bf16_dev_to_f64, sampled_gemm_check, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -44,10 +44,5 @@ def test_dgrad_wgrad(M, Nw, Kw):
         ref, mag = oracle.gemm_ref(at, bt)
         assert_gemm_close(bf16_dev_to_f64(dW), ref, mag, f"mx wgrad {M}x{Nw}x{Kw}")
     else:
-        rng = np.random.default_rng(4)
-        ms, ns = rng.integers(0, M, 384), rng.integers(0, Kw, 384)
-        ref, mag = oracle.gemm_ref_sampled(a, b, ms, ns)
-        assert_gemm_close(bf16_dev_to_f64(dX)[ms, ns], ref, mag, "mx dgrad full sampled")
-        ns2, ks = rng.integers(0, Nw, 384), rng.integers(0, Kw, 384)
-        ref, mag = oracle.gemm_ref_sampled(at, bt, ns2, ks)
-        assert_gemm_close(bf16_dev_to_f64(dW)[ns2, ks], ref, mag, "mx wgrad full sampled")
+        sampled_gemm_check(dX, a, b, "mx dgrad full sampled", seed=4)
+        sampled_gemm_check(dW, at, bt, "mx wgrad full sampled", seed=5)

@@ -10,7 +10,7 @@ import torch
 import block_scaled_fp8_e4m3_gb300 as fp8
 import oracle
 from block_scaled_fp8_e4m3_gb300 import synth
-from gpu_util import DEV, assert_bytes_equal, assert_gemm_close, bf16_dev_to_f64, to_np
+from gpu_util import DEV, assert_bytes_equal, assert_gemm_close, bf16_dev_to_f64, sampled_gemm_check, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -132,12 +132,7 @@ def test_gemm_full_mlp_sampled():
     Y = fp8.gemm(qx, qw, "fwd")
     a = _deq(*_o(oracle.quant_group_1x128_pow2, X))
     b = _deq(*_o(oracle.quant_block_128x128_pow2, W))
-    rng = np.random.default_rng(12)
-    ms = rng.integers(0, X.shape[0], 512)
-    ns = rng.integers(0, W.shape[0], 512)
-    ref, mag = oracle.gemm_ref_sampled(a, b, ms, ns)
-    got = bf16_dev_to_f64(Y)[ms, ns]
-    assert_gemm_close(got, ref, mag, "pow2 fwd 8192x4096x12288 sampled")
+    sampled_gemm_check(Y, a, b, "pow2 fwd 8192x4096x12288 sampled", seed=12)
 
 
 def test_sync_round_trip():
