@@ -150,22 +150,22 @@ def time_kernel(fn, flush, reps, warmup=3):
 
 def gemm_traffic():
     """DRAM bytes (read + write) per launch of the step's GEMM, from the
-    committed ncu summary, or None when the kernel source has changed since
-    those counters were taken (the summary records the sha256 of gemm_blockwise.cu)."""
+    machine-readable ncu record under profiles/, or None when the kernel
+    source has changed since those counters were taken (the record holds the
+    sha256 of gemm_blockwise.cu)."""
     import hashlib
     here = os.path.dirname(os.path.abspath(__file__))
-    summary = os.path.join(here, "profiles", "k_gemm_blockwise_fused_mlp_8192x4096x12288.md")
+    record = os.path.join(here, "profiles", "k_gemm_blockwise_traffic.json")
     src = os.path.join(here, "block_scaled_fp8_e4m3_gb300", "csrc", "gemm_blockwise.cu")
     try:
-        text = open(summary).read()
+        with open(record) as f:
+            d = json.load(f)
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    except OSError:
+    except (OSError, ValueError):
         return None
-    fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(("traffic_bytes_per_launch:",
-                                                                                       "gemm_blockwise_cu_sha256:")))
-    if fields.get("gemm_blockwise_cu_sha256", "").strip() != digest or "traffic_bytes_per_launch" not in fields:
+    if d.get("gemm_blockwise_cu_sha256") != digest or "traffic_bytes_per_launch" not in d:
         return None
-    return int(fields["traffic_bytes_per_launch"].strip())
+    return int(d["traffic_bytes_per_launch"])
 
 
 # ------------------------------------------------------------------ our arm
@@ -573,7 +573,8 @@ def run_fp8_param_drift(args, dev):
     """Figure 12 of the SkyRL page on synthetic weights: the cumulative FP8
     displacement over many lr = 1e-6 sign updates, and the single-step
     cosine against the update size, for fp32 and power-of-two scales."""
-    from block_scaled_fp8_e4m3_gb300 import param_drift, synth
+    import param_drift
+    from block_scaled_fp8_e4m3_gb300 import synth
     n = args.drift_size
     w0 = synth.fp32_master((n, n), seed=80).to(dev)
     steps = args.drift_steps
@@ -623,6 +624,68 @@ def cpu_baseline_sample(X, W, rows_x, rows_w):
                                            f"fp64 GEMM {rows_x}x{K}x{rows_w}, pack+install the W slice")
 
 
+def oracle_kernel_timings(X, W, rows=1024, gemm_shape=(512, 1024)):
+    """Each of the oracle's quantizers (and the fused producers, the
+    fp8_param re-quantization and the sync pack + install), as it stands, on
+    a bounded slice of the dense-MLP inputs (rows x 4096), timed once on one
+    thread and once on all of this host's cores; the fp64 GEMM reference
+    (gemm_shape[0] x 4096 x gemm_shape[1]) on all cores.  Bytes are each
+    kernel's algorithmic bytes for that slice, as on the GPU."""
+    import oracle
+    from block_scaled_fp8_e4m3_gb300 import synth
+    oracle.load()
+    ncores = cores()
+    xs = synth.bf16_bits(X[:rows].contiguous())
+    ws = synth.bf16_bits(W[:rows].contiguous())
+    wf = np.ascontiguousarray(W[:rows].float().numpy())
+    gu = synth.bf16_bits(torch.cat([X[:rows], X[rows:2 * rows]], dim=1).contiguous())
+    gam = np.full((K,), 0x3F80, np.uint16)  # bf16 1.0
+    cx, sx = oracle.quant_group_1x128(xs)
+    cw, sw = oracle.quant_block_128x128(ws)
+    spec = [dict(tag=1, kind=oracle.KIND_FP8, recipe=oracle.RECIPE_BLOCKWISE, rows=rows, cols=K,
+                 layout=oracle.LAYOUT_BLOCK_128x128, data=cw, scales=sw)]
+    dst = [dict(spec[0], data=np.zeros_like(cw), scales=np.zeros_like(sw))]
+    payload_bytes = oracle.sync_payload_size(spec)
+
+    def sync_round_trip():
+        pay = oracle.sync_pack(spec)
+        assert oracle.sync_install(pay, dst) == 0
+
+    n = rows * K
+    cases = [
+        ("quant_group_1x128", lambda: oracle.quant_group_1x128(xs), n * (3 + 4 / 128)),
+        ("quant_group_128x1_T", lambda: oracle.quant_group_128x1_T(xs), n * (3 + 4 / 128)),
+        ("quant_block_128x128_with_T", lambda: oracle.quant_block_128x128(ws, transposed=True), n * (4 + 8 / 16384)),
+        ("quant_mx_1x32", lambda: oracle.quant_mx_1x32(ws), n * (3 + 1 / 32)),
+        ("quant_mx_32x1_T", lambda: oracle.quant_mx_32x1_T(xs), n * (3 + 1 / 32)),
+        ("requant_1x128_to_128x1_T", lambda: oracle.requant_1x128_to_128x1_T(cx, sx), n * (2 + 8 / 128)),
+        ("param_requant_fp32_master", lambda: oracle.quant_block_128x128_f32(wf), n * (5 + 4 / 16384)),
+        ("rmsnorm_quant", lambda: oracle.quant_group_1x128(oracle.rmsnorm(xs, gam, 1e-6)[0]), n * (3 + 4 / 128)),
+        ("swiglu_quant", lambda: oracle.quant_group_1x128(oracle.swiglu(gu)), n * (5 + 4 / 128)),
+        ("sync_pack_install", sync_round_trip, 4.0 * payload_bytes),
+    ]
+    out = {"cores": ncores, "slice": f"{rows} rows x {K} of X / W (dense-MLP workload)"}
+    for name, fn, nbytes in cases:
+        rec = {}
+        for label, th in (("threads_1", 1), ("threads_all", ncores)):
+            oracle.set_threads(th)
+            t0 = time.perf_counter()
+            fn()
+            dt = time.perf_counter() - t0
+            rec[label] = {"s": round(dt, 4), "GB/s": round(nbytes / dt / 1e9, 3)}
+        out[name] = rec
+    oracle.set_threads(ncores)
+    gm, gn = gemm_shape
+    a = oracle.dequant_group(cx[:gm], np.ascontiguousarray(sx[:, :gm]))
+    b = oracle.dequant_block(cw[:gn], np.ascontiguousarray(sw[:gn // 128]))
+    t0 = time.perf_counter()
+    oracle.gemm_ref(a, b)
+    dt = time.perf_counter() - t0
+    out["gemm_ref_fp64"] = {"shape": f"{gm}x{K}x{gn}", "threads_all": {"s": round(dt, 4),
+                            "TFLOP/s": round(2.0 * gm * gn * K / dt / 1e12, 5)}}
+    return out
+
+
 def cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -664,6 +727,8 @@ def main():
     ap.add_argument("--kernel-reps", type=int, default=20)
     ap.add_argument("--kernel", default=None, choices=sorted(KERNEL_CASES),
                     help="run only this kernel on its workload (for profilers); prints its timing")
+    ap.add_argument("--no-oracle-kernels", action="store_true",
+                    help="skip the per-kernel oracle timings of the cpu_baseline leg")
     ap.add_argument("--experiment", default=None, choices=["fp8_param_drift"],
                     help="run a measurement from the pages instead of the benchmark; prints one JSON line")
     ap.add_argument("--drift-size", type=int, default=4096)
@@ -857,6 +922,8 @@ def main():
         dt, fl, desc = cpu_baseline_sample(Xh, Wh, 4096, 6144)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle", "sample": desc,
                "seconds": round(dt, 2)}
+        if not args.no_oracle_kernels:
+            cpu["per_kernel"] = oracle_kernel_timings(Xh, Wh)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

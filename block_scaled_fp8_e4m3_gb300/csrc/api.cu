@@ -990,7 +990,24 @@ fp8_status fp8_sync_install_noalloc(const void* payload_dev, uint64_t bytes, con
     e = launch_sync_verify(pay, data_offset, total, table_sum, &sc->status, cs);
     if (e != cudaSuccess) return cuda_fail(e, "sync_install_noalloc verify");
     if (nseg > 0) {
-        k_sync_scatter_table<<<152 * 4, 256, 0, cs>>>(sc, nseg);
+        // grid: the 256-thread blocks the copy needs, capped by what is
+        // resident on this device at once (SM count x blocks per SM)
+        uint64_t chunks = 0;
+        for (int i = 0; i < nseg; ++i) chunks += (segs[i].bytes + 15) / 16;
+        static int resident[64] = {};
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e, "sync_install_noalloc device");
+        int& r = resident[dev & 63];
+        if (r == 0) {
+            int sms = 0, per_sm = 0;
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_sync_scatter_table, 256, 0);
+            r = (sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+        }
+        const uint64_t need = (chunks + 255) / 256;
+        const unsigned grid = (unsigned)(need < 1 ? 1 : (need < (uint64_t)r ? need : (uint64_t)r));
+        k_sync_scatter_table<<<grid, 256, 0, cs>>>(sc, nseg);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "sync_install_noalloc scatter");
     }

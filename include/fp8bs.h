@@ -265,8 +265,10 @@ int64_t fp8_mx_grouped_scale_bytes(int64_t total_rows, int64_t cols, int32_t num
  * layout MX_1x32_GROUPED with fp8_mx_grouped_scale_bytes() bytes of scales.
  * Requires cols % 128 == 0.  Out-of-range gather entries are skipped on the
  * device; rows whose group offsets break the rules above get their codes
- * but no scale words.  Both are reported as FP8_ERR_INVALID_ARG by
- * fp8_status_poll(), and nothing is written outside dst. */
+ * row copied but no scale words.  Both are reported as FP8_ERR_INVALID_ARG by
+ * fp8_status_poll().  After such a report dst is partly written (some code
+ * rows copied, some scale words not), so its contents must not be used;
+ * every write of the call stays inside dst. */
 fp8_status fp8_permute_rows_mx(const fp8_tensor* src, const int32_t* gather_dev,
                                const int32_t* m_offsets_dev, int32_t num_groups,
                                const fp8_tensor* dst, fp8_stream_t stream);
@@ -409,8 +411,8 @@ fp8_status fp8_sync_install(const void* payload_dev, uint64_t bytes, const fp8_s
  * device looks up the array's device address; make that first call before
  * any stream capture.  Every call shares the array; calls are ordered on
  * the device as for fp8_sync_install (the same per-device event), so calls
- * from other streams or host threads do not overlap -- except inside a
- * stream capture, where the ordering is the caller's.
+ * from other streams or host threads do not overlap on the GPU; calls that
+ * did overlap there would race on the array.
  * Unlike fp8_sync_install it waits for the copy to finish and reports a
  * checksum mismatch directly (FP8_ERR_CHECKSUM, nothing written); header or
  * table mismatches return FP8_ERR_BAD_PAYLOAD before anything is enqueued.

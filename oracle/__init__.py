@@ -64,6 +64,8 @@ def load():
         "oracle_sync_payload_size": (C.c_uint64, [_P, C.c_int32]),
         "oracle_sync_pack": (C.c_uint64, [_P, C.c_int32, _P, C.c_uint64]),
         "oracle_sync_install": (C.c_int32, [_P, C.c_uint64, _P, C.c_int32]),
+        "oracle_set_threads": (None, [C.c_int32]),
+        "oracle_max_threads": (C.c_int32, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -71,6 +73,15 @@ def load():
         fn.argtypes = args
     _lib = lib
     return lib
+
+
+def set_threads(n: int) -> None:
+    """Thread count of the oracle's OpenMP loops (timing only)."""
+    load().oracle_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(load().oracle_max_threads())
 
 
 def _ptr(a: np.ndarray):

@@ -49,6 +49,7 @@
 #include <string.h>
 #include <math.h>
 #include <stdlib.h>
+#include <omp.h>
 
 /* ------------------------------------------------------------------------ */
 /* Scalar formats                                                            */
@@ -1016,4 +1017,16 @@ int32_t oracle_sync_install(const uint8_t* payload, uint64_t bytes,
     free(doff);
     free(soff);
     return rc;
+}
+
+/* Thread count of the OpenMP loops above (timing of the oracle on one
+ * thread and on all cores; no effect on any result). */
+void oracle_set_threads(int32_t n)
+{
+    omp_set_num_threads(n > 0 ? n : 1);
+}
+
+int32_t oracle_max_threads(void)
+{
+    return omp_get_max_threads();
 }

@@ -7,7 +7,8 @@ over many steps, in units of the master's own displacement; right: the
 cosine similarity between one master update and the change it causes in the
 FP8 storage, against the update's size.  The steps run through
 ``param_requantize`` (the fused W += dW and Q(W) kernel); the analysis below
-(dequantization, sums) is plain torch on the device.
+(dequantization, sums) is plain torch on the device: an experiment run by
+``bench.py --experiment fp8_param_drift``, kept outside the library package.
 
 Readings: the updates are Adam-like, lr * (+-1) with independent fair signs;
 "displacement normalized by the master's" is taken as the projection
@@ -20,7 +21,7 @@ from __future__ import annotations
 
 import torch
 
-from . import LAYOUT_MX_1x32, QTensor, param_requantize, synth
+from block_scaled_fp8_e4m3_gb300 import LAYOUT_MX_1x32, QTensor, param_requantize, synth
 
 
 def dequantize_block(q: QTensor) -> torch.Tensor:

@@ -11,7 +11,8 @@ import torch
 
 import block_scaled_fp8_e4m3_gb300 as fp8
 import oracle
-from block_scaled_fp8_e4m3_gb300 import param_drift, synth
+import param_drift
+from block_scaled_fp8_e4m3_gb300 import synth
 from gpu_util import DEV, assert_bytes_equal, to_np
 
 pytestmark = pytest.mark.gpu
