@@ -38,6 +38,7 @@ struct alignas(16) Barriers {
     uint64_t acc_full[4];
     uint64_t acc_empty[4];
     uint64_t drain;
+    uint64_t sf_ready[kMaxStages];  // MX: the stage's scale factors copied into TMEM
     uint32_t tmem_base;
     int abort;
     int num_mtiles;  // MX: total 256-row cluster tiles over all groups

@@ -19,6 +19,9 @@ namespace {
 // each CTA stages its 128 rows of A, its 128 of the tile's 256 rows of B, the
 // scale atom of its A rows and both scale atoms of the tile's B rows.
 constexpr int kMxBN = 256;
+constexpr int kMxEpiWarps = 8;                        // warps 2..9
+constexpr int kMxSfWarp = kEpiWarp0 + kMxEpiWarps;    // copies the scale factors into TMEM
+constexpr int kMxThreads = (kMxSfWarp + 1) * 32;      // 352
 constexpr int kMxStages = 6;
 constexpr uint32_t kMxStageBytes = (BM + kMxBN / 2) * BK;  // 32 KB
 constexpr uint32_t kSfStageBytes = 1536;                    // SFA atom + two SFB atoms
@@ -127,7 +130,7 @@ __device__ __forceinline__ TileCoord mx_tile(int tile, int tiles_n, const int* p
     return c;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kMxThreads, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB, const MxParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -152,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bar->acc_full[0], 1);
         mbar_init(&bar->acc_empty[0], 2 * (kEpiThreads / 32));
+        for (int st = 0; st < kMxStages; ++st) mbar_init(&bar->sf_ready[st], 1);
         mbar_init(&bar->drain, 1);
         bar->abort = 0;
         fence_mbar_init();
@@ -262,19 +266,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int tile = cid; tile < num_tiles && ok; tile += ncl) {
                 if (!mbar_wait_bounded(&bar->acc_empty[0], aph ^ 1, abort, p.st, 12)) break;
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait_bounded(&bar->full[s], ph, abort, p.st, 13)) {
+                    // the stage's operands landed and its scale factors are in
+                    // TMEM (copied by the scale-factor warp)
+                    if (!mbar_wait_bounded(&bar->full[s], ph, abort, p.st, 13) ||
+                        !mbar_wait_bounded(&bar->sf_ready[s], ph, abort, p.st, 15)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + s * kMxStageBytes);
-                    const uint32_t sf_addr = smem_u32(sf + s * kSfStageBytes);
                     const uint32_t tsfa = tmem + sf_col0 + 16u * s;
                     const uint32_t tsfb = tsfa + 4;
-                    // each CTA copies its own shared-memory scales into its own TMEM
-                    tc_cp_pair_32x128b_warpx4(tsfa, sdesc_sf_32x16(sf_addr));
-                    tc_cp_pair_32x128b_warpx4(tsfb, sdesc_sf_32x16(sf_addr + 512));
-                    tc_cp_pair_32x128b_warpx4(tsfb + 4, sdesc_sf_32x16(sf_addr + 1024));
                     const uint64_t adesc = sdesc_k_sw128(a_addr);
                     const uint64_t bdesc = sdesc_k_sw128(a_addr + BM * BK);
 #pragma unroll
@@ -293,6 +295,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_commit_pair(&bar->drain, 1);
             mbar_wait_drain(&bar->drain, 0, p.st);
+        }
+    } else if (warp == kMxSfWarp) {
+        // scale factors: per stage, each CTA's A atom and the tile's two B
+        // atoms copied shared -> TMEM (tcgen05.cp, issued by the leader for
+        // both CTAs), then sf_ready[s].  A thread issues a tcgen05 instruction
+        // every ~60 cycles, so these three copies on the MMA thread would
+        // stretch every K block; here they run one or more stages ahead.
+        // Stage s's TMEM slot was last read by the MMAs of the K block six
+        // earlier, which completed before the producer refilled stage s.
+        if (lane == 0 && rank == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int tile = cid; tile < num_tiles && ok; tile += ncl) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait_bounded(&bar->full[s], ph, abort, p.st, 16)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sf_addr = smem_u32(sf + s * kSfStageBytes);
+                    const uint32_t tsfa = tmem + sf_col0 + 16u * s;
+                    const uint32_t tsfb = tsfa + 4;
+                    // each CTA copies its own shared-memory scales into its own TMEM
+                    tc_cp_pair_32x128b_warpx4(tsfa, sdesc_sf_32x16(sf_addr));
+                    tc_cp_pair_32x128b_warpx4(tsfb, sdesc_sf_32x16(sf_addr + 512));
+                    tc_cp_pair_32x128b_warpx4(tsfb + 4, sdesc_sf_32x16(sf_addr + 1024));
+                    tc_commit_pair(&bar->sf_ready[s], 1);
+                    if (++s == kMxStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
         }
     } else if (warp >= kEpiWarp0) {
         const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
@@ -408,7 +444,7 @@ cudaError_t launch_gemm_mx(const GemmMxArgs& a, StatusBlock* status, cudaStream_
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (unsigned)tiles);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kMxThreads);
     cfg.dynamicSmemBytes = kSmemMx;
     cfg.stream = st;
     cfg.attrs = attr;
