@@ -217,13 +217,14 @@ __global__ void __launch_bounds__(256, 5) k_quant_group_m(const uint16_t* __rest
 // fp32, x' = RN(dec(q) s_row) (the E4M3 -> f16 conversion is exact), and x'
 // is quantized in 128x1 groups with the codes transposed.  The tiling is that
 // of k_quant_group_m (128 rows x 64 columns, one 1x128 scale per row); x' has
-// a full fp32 significand, so scales and quotients are IEEE divisions.
+// a full fp32 significand: the scales are IEEE divisions and the quotients
+// come from neg_quotient2_exact (the IEEE quotient bit for bit).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256, 5) k_requant_group_m(const uint8_t* __restrict__ codes, const float* __restrict__ rs,
                                                          int64_t M, int64_t K, uint8_t* __restrict__ codes_t,
                                                          float* __restrict__ scales_t) {
     __shared__ float red[8][64];
-    __shared__ float col_scale[64];
+    __shared__ float col_scale[64], col_nrcp[64];
     __shared__ uint32_t tile[64 * 33];
 
     const int64_t ctiles = K / 64;
@@ -272,15 +273,24 @@ __global__ void __launch_bounds__(256, 5) k_requant_group_m(const uint8_t* __res
         for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w][t]);
         const float sc = group_scale(a);
         col_scale[t] = sc;
+        col_nrcp[t] = -__frcp_rn(sc);
         scales_t[mb * K + c0 + t] = sc;
     }
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const float sc = col_scale[chunk * 8 + j];
-        tile[(chunk * 8 + j) * 33 + quad] =
-            e4m3x2(__fdiv_rn(f[0][j], sc), __fdiv_rn(f[1][j], sc)) |
-            (e4m3x2(__fdiv_rn(f[2][j], sc), __fdiv_rn(f[3][j], sc)) << 16);
+        uint32_t word;
+        if (sc >= 0x1p-90f && sc <= 0x1p126f) {
+            float n[4];
+            neg_quotient2_exact(f[0][j], f[1][j], sc, col_nrcp[chunk * 8 + j], n[0], n[1]);
+            neg_quotient2_exact(f[2][j], f[3][j], sc, col_nrcp[chunk * 8 + j], n[2], n[3]);
+            word = (e4m3x2(n[0], n[1]) | (e4m3x2(n[2], n[3]) << 16)) ^ 0x80808080u;  // codes of -n: sign back
+        } else {
+            word = e4m3x2(__fdiv_rn(f[0][j], sc), __fdiv_rn(f[1][j], sc)) |
+                   (e4m3x2(__fdiv_rn(f[2][j], sc), __fdiv_rn(f[3][j], sc)) << 16);
+        }
+        tile[(chunk * 8 + j) * 33 + quad] = word;
     }
     __syncthreads();
 #pragma unroll
@@ -402,7 +412,8 @@ __global__ void __launch_bounds__(256) k_quant_block(const uint16_t* __restrict_
 // access).  With kDelta the step's final add W += dW (fp32, round to
 // nearest) is applied first and written back.  fp32 recipe: s = RN(amax/448),
 // 1 when that is 0; codes from the IEEE quotient w/s (fp32 inputs have full
-// 24-bit significands, so the division is the IEEE one).  Power-of-two
+// 24-bit significands: neg_quotient2_exact, the IEEE quotient bit for bit,
+// or the IEEE division itself for scales outside its range).  Power-of-two
 // recipe: e from RN(amax/448), codes from the exact product w * 2^-e.
 // ---------------------------------------------------------------------------
 template <bool kPow2, bool kDelta>
@@ -473,16 +484,22 @@ __global__ void __launch_bounds__(256, 3) k_param_requant(float* __restrict__ ma
         }
     }
     uint8_t* crow = codes + (n0 + warp * 16) * K + k0 + lane * 4;
+    const bool exact = !kPow2 && s >= 0x1p-90f && s <= 0x1p126f;
+    const float nr = exact ? -__frcp_rn(s) : 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        float q0, q1, q2, q3;
+        uint32_t c;
         if (kPow2) {
-            q0 = v[i].x * mul; q1 = v[i].y * mul; q2 = v[i].z * mul; q3 = v[i].w * mul;
+            c = e4m3x2(v[i].x * mul, v[i].y * mul) | (e4m3x2(v[i].z * mul, v[i].w * mul) << 16);
+        } else if (exact) {
+            float n0, n1, n2, n3;
+            neg_quotient2_exact(v[i].x, v[i].y, s, nr, n0, n1);
+            neg_quotient2_exact(v[i].z, v[i].w, s, nr, n2, n3);
+            c = (e4m3x2(n0, n1) | (e4m3x2(n2, n3) << 16)) ^ 0x80808080u;  // codes of -n: sign back
         } else {
-            q0 = __fdiv_rn(v[i].x, s); q1 = __fdiv_rn(v[i].y, s);
-            q2 = __fdiv_rn(v[i].z, s); q3 = __fdiv_rn(v[i].w, s);
+            c = e4m3x2(__fdiv_rn(v[i].x, s), __fdiv_rn(v[i].y, s)) |
+                (e4m3x2(__fdiv_rn(v[i].z, s), __fdiv_rn(v[i].w, s)) << 16);
         }
-        const uint32_t c = e4m3x2(q0, q1) | (e4m3x2(q2, q3) << 16);
         *reinterpret_cast<uint32_t*>(crow + i * K) = c;
         if (codes_t) *reinterpret_cast<uint32_t*>(tile + (warp * 16 + i) * kStride + lane * 4) = c;
     }

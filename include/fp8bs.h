@@ -162,8 +162,11 @@ fp8_status fp8_quantize_group(const void* x_bf16, int64_t M, int64_t K, int64_t 
  *  in:  FP8_RECIPE_BLOCKWISE_FP32, FP8_LAYOUT_GROUP_1x128, rows M, cols K.
  *  out: FP8_RECIPE_BLOCKWISE_FP32, FP8_LAYOUT_GROUP_1x128, rows K, cols M
  *       (codes [K][M], scales fp32 [M/128][K]).
- * Requires M % 128 == 0, K % 128 == 0.  Scales and quotients are IEEE fp32
- * divisions (x' has a full fp32 significand). */
+ * Requires M % 128 == 0, K % 128 == 0.  Scales are IEEE fp32 divisions; the
+ * codes are those of the IEEE fp32 quotients x' / s (x' has a full fp32
+ * significand).  An E4M3 NaN code in `in` (0x7F, 0xFF; never written by the
+ * quantizers here) gives a NaN code, of either sign, at its transposed
+ * position, and does not enter its group's scale. */
 fp8_status fp8_requantize_transposed(const fp8_tensor* in, const fp8_tensor* out, fp8_stream_t stream);
 
 /* 128x128 block quantization of a bf16 weight w [N][ld] (first K columns).

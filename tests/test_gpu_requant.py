@@ -85,3 +85,21 @@ def test_quotients_at_rounding_midpoints():
     xd = (oracle.e4m3_decode(codes).astype(np.float32) * srow[0][:, None]).astype(np.float32)
     naive = oracle.e4m3_encode((xd * np.repeat(np.float32(1) / st, 128, axis=0)).astype(np.float32))
     assert (naive.T != ct).any()
+
+
+def test_random_row_scales_full_significands():
+    """Saved codes with arbitrary fp32 row scales (full significands,
+    log-uniform over 2^-24..2^24, so every quotient x' / s has a full
+    significand too) and all finite codes: codes and scales byte-equal to the
+    oracle over 2048 x 1024, which spans 16 x 16 tiles of the kernel."""
+    rng = np.random.default_rng(1234)
+    M, K = 2048, 1024
+    codes = rng.integers(0, 256, size=(M, K), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] ^= 0x01                        # no NaN codes: 0x7F -> 0x7E
+    srow = np.exp2(rng.uniform(-24.0, 24.0, size=(K // 128, M))).astype(np.float32)
+    q = fp8.QTensor(torch.from_numpy(codes).to(DEV), torch.from_numpy(srow).to(DEV), M, K, fp8.RECIPE_BLOCKWISE,
+                    fp8.LAYOUT_GROUP_1x128)
+    qt = fp8.requantize_transposed(q)
+    ct, st = oracle.requant_1x128_to_128x1_T(codes, srow)
+    assert_bytes_equal(to_np(qt.codes), ct, "codes^T")
+    assert_bytes_equal(to_np(qt.scales), st, "scales")
