@@ -132,7 +132,11 @@ class Flusher:
 
 
 def time_kernel(fn, flush, reps, warmup=3):
-    """Median device time (ms) of fn() over reps, L2 flushed before each."""
+    """Device time (ms) of fn(), L2 flushed before each launch: the mean of
+    reps CUDA-event pairs with the lowest and highest 10 % dropped.  The
+    events' clock ticks in steps of about 2 us on this GPU, so a median of
+    ~20 us launches would sit on that grid; the mean of many pairs, whose
+    start falls at random within a tick, does not."""
     for _ in range(warmup):
         flush()
         fn()
@@ -145,7 +149,9 @@ def time_kernel(fn, flush, reps, warmup=3):
         e1.record()
         ts.append((e0, e1))
     torch.cuda.synchronize()
-    return float(np.median([a.elapsed_time(b) for a, b in ts]))
+    d = np.sort([a.elapsed_time(b) for a, b in ts])
+    k = len(d) // 10
+    return float(np.mean(d[k:len(d) - k]))
 
 
 def gemm_traffic():
@@ -724,7 +730,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-breakdown", action="store_true", help="skip the per-kernel table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-reps", type=int, default=20)
+    ap.add_argument("--kernel-reps", type=int, default=40)
     ap.add_argument("--kernel", default=None, choices=sorted(KERNEL_CASES),
                     help="run only this kernel on its workload (for profilers); prints its timing")
     ap.add_argument("--no-oracle-kernels", action="store_true",
