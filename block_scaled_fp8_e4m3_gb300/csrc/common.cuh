@@ -82,45 +82,53 @@ __device__ __forceinline__ float group_scale_bf16(float amax) {
     return amax == 0.0f ? 1.0f : (amax <= 3.402823466e38f ? s : amax);
 }
 
-// x / s correctly rounded, for the quotients of the blockwise quantizers:
-// x a bf16 value and s = RN(amax / 448) of the group maximum amax >= |x|.
-// For s >= 2^-100 it takes Markstein's FMA correction of the product with the
-// correctly rounded reciprocal (P. Markstein, "Computation of elementary
-// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
-// 1990): q0 = RN(x r), e = x - s q0 (exact by FMA), q = RN(q0 + e r), with the
-// sign of x so that -0 stays -0.  An exhaustive host check over every bf16 x
-// and every bf16 group maximum gives the E4M3 code of the IEEE quotient in
-// every case (the quotient bits differ only below 2^-11, where the code is
-// zero either way); smaller or non-finite s take the IEEE division.
+// x / s for the quotients of the blockwise quantizers: x a bf16 value and
+// s = RN(amax / 448) of the group maximum amax >= |x|.  For s >= 2^-100 it
+// takes Markstein's FMA correction of the product with the correctly rounded
+// reciprocal (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q0 = RN(x r),
+// e = x - s q0 (exact by FMA), q = RN(q0 + e r).  An exhaustive host check
+// over every bf16 x and every bf16 group maximum gives the E4M3 code of the
+// IEEE quotient in every case (the quotient bits differ only below 2^-11,
+// where the code is zero either way); smaller or non-finite s take the IEEE
+// division.
 struct Divider {
-    float s, r;
+    float s, nr;  // nr = -RN(1/s)
     bool fast;
 };
 
 __device__ __forceinline__ Divider make_divider(float s) {
     Divider d;
     d.s = s;
-    d.r = __frcp_rn(s);
+    d.nr = -__frcp_rn(s);
     d.fast = s >= 0x1p-100f && s <= 3.402823466e38f;
     return d;
 }
 
-// Two such quotients at once with packed fp32x2 arithmetic (each half
-// rounded as above); d.fast must hold.
-__device__ __forceinline__ void quotient2_fast(const Divider& d, float x0, float x1, float& q0, float& q1) {
-    uint64_t xs, q;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(xs) : "f"(x0), "f"(x1));
-    asm("{\n\t.reg .b64 r2, s2, p, e;\n\t"
-        "mov.b64 r2, {%2, %2};\n\tmov.b64 s2, {%3, %3};\n\t"
-        "mul.rn.f32x2 p, %1, r2;\n\t"
-        "fma.rn.f32x2 e, s2, p, %1;\n\t"
-        "fma.rn.f32x2 %0, e, r2, p;\n\t}\n"
-        : "=l"(q)
-        : "l"(xs), "f"(d.r), "f"(-d.s));
-    float a, b;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(q));
-    q0 = copysignf(a, x0);
-    q1 = copysignf(b, x1);
+// The codes of x0..x3 / s as above (four E4M3 bytes, x0 in the lowest);
+// d.fast must hold.  The correction runs on the negated quotient, two values
+// per packed instruction: n = RN(x nr), e = x + n s (exact), -q = RN(n + e nr).
+// A zero x then ends as a zero of the opposite sign (RN(+0 + -0) = +0 and
+// RN(-0 + -0) = -0), so flipping the sign bits of the four codes gives the
+// codes of q with the sign of x, -0 included, and no copysign per value.
+__device__ __forceinline__ uint32_t codes4_div_fast(const Divider& d, float x0, float x1, float x2, float x3) {
+    uint64_t a, b, na, nb;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(x0), "f"(x1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(x2), "f"(x3));
+    asm("{\n\t.reg .b64 r2, s2, e;\n\t"
+        "mov.b64 r2, {%4, %4};\n\tmov.b64 s2, {%5, %5};\n\t"
+        "mul.rn.f32x2 %0, %2, r2;\n\t"
+        "mul.rn.f32x2 %1, %3, r2;\n\t"
+        "fma.rn.f32x2 e, %0, s2, %2;\n\t"
+        "fma.rn.f32x2 %0, e, r2, %0;\n\t"
+        "fma.rn.f32x2 e, %1, s2, %3;\n\t"
+        "fma.rn.f32x2 %1, e, r2, %1;\n\t}\n"
+        : "=&l"(na), "=&l"(nb)
+        : "l"(a), "l"(b), "f"(d.nr), "f"(d.s));
+    float n0, n1, n2, n3;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(n0), "=f"(n1) : "l"(na));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(n2), "=f"(n3) : "l"(nb));
+    return (e4m3x2(n0, n1) | (e4m3x2(n2, n3) << 16)) ^ 0x80808080u;
 }
 
 // MX shared exponent e = clamp(floor(log2 amax) - 8, -127, 127) from the fp32

@@ -25,6 +25,7 @@
 //  * setmaxnreg gives the four epilogue warpgroups 112 registers and the
 //    control warpgroup (TMA, two MMA issuers, scale loader) 32.
 #include "gemm_common.cuh"
+#include "quant_common.cuh"
 
 namespace fp8bs {
 
@@ -449,22 +450,15 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                             uint32_t cw[kBwHalfCols / 4];
 #pragma unroll
                             for (int i = 0; i < kBwHalfCols / 8; ++i) {
-                                float f[8], qv[8];
+                                float f[8];
 #pragma unroll
                                 for (int k = 0; k < 4; ++k) {
                                     f[2 * k] = bf16_lo(packed[4 * i + k]);
                                     f[2 * k + 1] = bf16_hi(packed[4 * i + k]);
                                 }
-                                if (dv.fast) {
-#pragma unroll
-                                    for (int k = 0; k < 4; ++k)
-                                        quotient2_fast(dv, f[2 * k], f[2 * k + 1], qv[2 * k], qv[2 * k + 1]);
-                                } else {
-#pragma unroll
-                                    for (int k = 0; k < 8; ++k) qv[k] = __fdiv_rn(f[k], dv.s);
-                                }
-                                cw[2 * i] = e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
-                                cw[2 * i + 1] = e4m3x2(qv[4], qv[5]) | (e4m3x2(qv[6], qv[7]) << 16);
+                                const uint2 c = encode8_div(f, dv);
+                                cw[2 * i] = c.x;
+                                cw[2 * i + 1] = c.y;
                             }
                             if (p.q_v8) {
                                 st_v8(codes, cw);

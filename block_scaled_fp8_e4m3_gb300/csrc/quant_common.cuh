@@ -30,17 +30,17 @@ __device__ __forceinline__ float amax8(const float (&f)[8]) {
 
 // 8 values divided by s (the IEEE fp32 quotient) and encoded: 8 codes in two words.
 __device__ __forceinline__ uint2 encode8_div(const float (&f)[8], const Divider& d) {
-    float q[8];
+    uint2 r;
     if (d.fast) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) quotient2_fast(d, f[2 * k], f[2 * k + 1], q[2 * k], q[2 * k + 1]);
+        r.x = codes4_div_fast(d, f[0], f[1], f[2], f[3]);
+        r.y = codes4_div_fast(d, f[4], f[5], f[6], f[7]);
     } else {
+        float q[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) q[k] = __fdiv_rn(f[k], d.s);
+        r.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
+        r.y = e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16);
     }
-    uint2 r;
-    r.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
-    r.y = e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16);
     return r;
 }
 

@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(256, 5) k_quant_group_m(const uint16_t* __rest
                                                        int64_t ld, uint8_t* __restrict__ codes_t,
                                                        void* __restrict__ scales) {
     __shared__ float red[8][64];
-    __shared__ float col_scale[64], col_rcp[64];
+    __shared__ float col_scale[64], col_nrcp[64];
     __shared__ uint32_t tile[64 * 33];
 
     const int64_t ctiles = (K + 63) / 64;
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(256, 5) k_quant_group_m(const uint16_t* __rest
         } else {
             const float s = group_scale_bf16(a);
             col_scale[t] = s;
-            col_rcp[t] = __frcp_rn(s);
+            col_nrcp[t] = -__frcp_rn(s);
             if (c0 + t < K) static_cast<float*>(scales)[mb * K + c0 + t] = s;
         }
     }
@@ -183,15 +183,14 @@ __global__ void __launch_bounds__(256, 5) k_quant_group_m(const uint16_t* __rest
         }
         Divider dv;
         dv.s = col_scale[chunk * 8 + j];
-        dv.r = col_rcp[chunk * 8 + j];
+        dv.nr = col_nrcp[chunk * 8 + j];
         dv.fast = dv.s >= 0x1p-100f && dv.s <= 3.402823466e38f;
         if (dv.fast) {
-            quotient2_fast(dv, f[0][j], f[1][j], q[0], q[1]);
-            quotient2_fast(dv, f[2][j], f[3][j], q[2], q[3]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) q[i] = __fdiv_rn(f[i][j], dv.s);
+            tile[(chunk * 8 + j) * 33 + quad] = codes4_div_fast(dv, f[0][j], f[1][j], f[2][j], f[3][j]);
+            continue;
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = __fdiv_rn(f[i][j], dv.s);
         tile[(chunk * 8 + j) * 33 + quad] = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
     }
     __syncthreads();

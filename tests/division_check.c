@@ -3,8 +3,10 @@
  * and make_divider in the CUDA sources).  First, s = RN(a / 448) for every
  * positive finite bf16 a, from a * RN(1/448) and one correction.  For every bf16 x and every positive finite bf16 group
  * maximum a >= |x|, with s = RN(a / 448) >= 2^-100:
- *   r = RN(1 / s), q0 = RN(x r), e = fma(-s, q0, x), q1 = copysign(fma(e, r, q0), x)
- * must give the same E4M3 code as the IEEE quotient RN(x / s).  The E4M3
+ *   nr = -RN(1 / s), n = RN(x nr), e = fma(n, s, x), n1 = fma(e, nr, n)
+ * (one correction, run on the negated quotient as the kernels do) must give,
+ * with the sign bit flipped, the same E4M3 code as the IEEE quotient
+ * RN(x / s), signed zeros included.  The E4M3
  * encoder here is a brute-force nearest search (ties to even mantissa,
  * saturating), independent of both.  Prints the counts; exit status 1 on
  * any code mismatch. */
@@ -67,18 +69,18 @@ int main(void) {
             slow_groups++;
             continue;
         }
-        const float r = 1.0f / s;
+        const float nr = -(1.0f / s);
         for (int xh = 0; xh < 0x10000; ++xh) {
             const float x = from_bf16((uint16_t)xh);
             if (!(fabsf(x) <= a)) continue;
             const float q = x / s;
-            const float q0 = x * r;
-            const float e = fmaf(-s, q0, x);
-            const float q1 = copysignf(fmaf(e, r, q0), x);
+            const float n0 = x * nr;
+            const float e = fmaf(n0, s, x);
+            const float n1 = fmaf(e, nr, n0);
             pairs++;
-            if (bits_of(q1) != bits_of(q)) {
+            if (bits_of(n1) != (bits_of(q) ^ 0x80000000u)) {
                 quotient_diffs++;
-                if (e4m3_code(q1) != e4m3_code(q)) code_diffs++;
+                if ((e4m3_code(n1) ^ 0x80) != e4m3_code(q)) code_diffs++;
             }
         }
     }

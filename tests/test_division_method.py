@@ -4,7 +4,8 @@ The blockwise quantizers encode the fp32 quotient x / s (s = amax / 448, the
 "AIS: Adaptive Importance Sampling for Quantized RL" explainer, equation
 Q(X)).  The CUDA kernels form s from amax * RN(1/448), and x / s from
 x * RN(1/s), each with one FMA correction (Markstein's method; the latter
-when s >= 2^-100).  This test compiles a host restatement
+when s >= 2^-100, run on the negated quotient so that a zero keeps its
+sign).  This test compiles a host restatement
 of that formula and checks it against the IEEE quotient over every bf16 input
 and every bf16 group maximum: the E4M3 codes must agree everywhere.
 """
