@@ -524,6 +524,25 @@ def _case_quant(kind):
             qxe = fp8.quantize_mx(Xe)
             qa = fp8.permute_rows_mx(qxe, gather, offsets)
             return lambda: fp8.permute_rows_mx(qxe, gather, offsets, out=qa), None
+        if kind in ("sync_split", "sync_noalloc"):
+            # the same W as 48 entries of 256 rows: 96 segments, more than one
+            # copy table holds, so the install takes the two-kernel path
+            # (verify, then copy); or the whole W through the allocation-free
+            # entry point (verify, then a table-driven copy)
+            W = synth.mlp().tensors["W"].to(dev)
+            qw = fp8.quantize_block(W)
+            parts = 48 if kind == "sync_split" else 1
+            rows = qw.rows // parts
+            ents = [fp8.SyncEntry(i + 1, fp8.QTensor(qw.codes[i * rows:(i + 1) * rows],
+                                                     qw.scales[i * rows // 128:(i + 1) * rows // 128], rows, qw.cols,
+                                                     qw.recipe, qw.layout)) for i in range(parts)]
+            payload = fp8.sync_pack(ents)
+            dst = [fp8.SyncEntry(e.tag, fp8.QTensor(torch.empty_like(e.tensor.codes), torch.empty_like(e.tensor.scales),
+                                                   e.tensor.rows, e.tensor.cols, e.tensor.recipe, e.tensor.layout))
+                   for e in ents]
+            if kind == "sync_noalloc":
+                return lambda: fp8.sync_install_noalloc(payload, dst), None
+            return lambda: fp8.sync_install(payload, dst, check=False), None
         if kind in ("sync_pack", "sync_install"):
             W = synth.mlp().tensors["W"].to(dev)
             qw = fp8.quantize_block(W)
@@ -571,6 +590,7 @@ KERNEL_CASES = {
     "param_requant": _case_quant("param"), "param_update_requant_with_T": _case_quant("param_update"),
     "rmsnorm_quant": _case_quant("rmsnorm"), "swiglu_quant": _case_quant("swiglu"),
     "sync_pack": _case_quant("sync_pack"), "sync_install": _case_quant("sync_install"), "permute_rows_mx": _case_quant("permute"),
+    "sync_install_split": _case_quant("sync_split"), "sync_install_noalloc": _case_quant("sync_noalloc"),
     "dispatch_quantize_mx": _case_quant("permute_quant"),
 }
 
