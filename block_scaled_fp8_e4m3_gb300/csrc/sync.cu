@@ -32,12 +32,15 @@ struct SegTable {
     int n;
 };
 
-// chunk c of 16 bytes -> (segment, chunk within segment) by a scan of the
-// per-segment chunk counts
+// chunk c of 16 bytes -> its segment: the last s with start[s] <= c, by
+// binary search over the per-segment chunk offsets (up to 32 segments)
 __device__ __forceinline__ int find_seg(const uint64_t* start, int n, uint64_t c) {
-    int s = 0;
-    while (s + 1 < n && start[s + 1] <= c) ++s;
-    return s;
+    int lo = 0, hi = n;  // start[lo] <= c < start[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (start[mid] <= c) lo = mid; else hi = mid;
+    }
+    return lo;
 }
 
 __device__ __forceinline__ uint4 load16_tail(const uint8_t* src, uint64_t off, uint64_t bytes) {
