@@ -143,32 +143,39 @@ __device__ __forceinline__ unsigned long long verify_part(const uint8_t* __restr
     }
     const uint64_t c0 = data_offset / 16, c1 = total_bytes / 16;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    const uint4* p4 = reinterpret_cast<const uint4*>(payload);
     unsigned long long sum = 0;
-    // the next round's loads are issued before this round is mixed
+    auto mix_chunk = [&](const uint4& v, uint64_t cc) {
+        const unsigned long long w0 = (unsigned long long)v.x | ((unsigned long long)v.y << 32);
+        const unsigned long long w1 = (unsigned long long)v.z | ((unsigned long long)v.w << 32);
+        sum += mix64(w0 ^ (2 * cc)) + mix64(w1 ^ (2 * cc + 1));
+    };
+    // whole rounds of kUnroll chunks: one bounds check per round, and the
+    // next round's loads issued before this round is mixed
     uint64_t c = c0 + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    uint4 v[kUnroll];
+    const uint64_t span = (kUnroll - 1) * stride;
+    if (c + span < c1) {
+        uint4 v[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-        if (c + u * stride < c1) v[u] = *reinterpret_cast<const uint4*>(payload + (c + u * stride) * 16);
-    for (; c < c1; c += kUnroll * stride) {
-        uint4 nv[kUnroll];
+        for (int u = 0; u < kUnroll; ++u) v[u] = p4[c + u * stride];
+        while (true) {
+            const uint64_t cn = c + kUnroll * stride;
+            const bool more = cn + span < c1;
+            uint4 nv[kUnroll];
+            if (more) {
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const uint64_t cn = c + (kUnroll + u) * stride;
-            if (cn < c1) nv[u] = *reinterpret_cast<const uint4*>(payload + cn * 16);
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const uint64_t cc = c + u * stride;
-            if (cc < c1) {
-                const unsigned long long w0 = (unsigned long long)v[u].x | ((unsigned long long)v[u].y << 32);
-                const unsigned long long w1 = (unsigned long long)v[u].z | ((unsigned long long)v[u].w << 32);
-                sum += mix64(w0 ^ (2 * cc)) + mix64(w1 ^ (2 * cc + 1));
+                for (int u = 0; u < kUnroll; ++u) nv[u] = p4[cn + u * stride];
             }
-        }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = nv[u];
+            for (int u = 0; u < kUnroll; ++u) mix_chunk(v[u], c + u * stride);
+            c = cn;
+            if (!more) break;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) v[u] = nv[u];
+        }
     }
+    // this thread's last chunks (fewer than kUnroll)
+    for (; c < c1; c += stride) mix_chunk(p4[c], c);
     return block_sum(sum);
 }
 
