@@ -117,15 +117,65 @@ __device__ __forceinline__ void quant_group16(const float (&y)[8], bool ok, int 
 // ---------------------------------------------------------------------------
 // RMSNorm + quantization.  A row is split into segments of 1024 elements,
 // one warp each (kW warps per row, a power of two >= K/1024; 8/kW rows per
-// 256-thread block).  Lane l of a warp holds chunks j < 4 of its segment:
-// elements 1024 seg + 256 j + 8 l .. + 7 (each chunk is one 512-byte warp
-// access; K % 128 == 0, so a chunk is whole, half or empty).  The sum of
+// 256-thread block).  A segment is two rounds of four 128-element groups,
+// eight lanes per group: lane (gq = l/8, sub = l%8) holds elements
+// 8 sub .. 8 sub + 7 and 64 + 8 sub .. 64 + 8 sub + 7 of group gq of each
+// round (so each 16-byte load instruction of the warp covers four whole
+// 128-byte lines), 16 values of one group per lane and round.  The sum of
 // squares is accumulated in fp32 per lane, reduced over the warp, and the kW
 // warp partials of a row are added in segment order through shared memory
 // (every warp of the row gets the same sum); rstd = RN(1/sqrt(RN(ss/K) +
-// eps)), y = RN_bf16(RN(x rstd) gamma).
+// eps)), y = RN_bf16(RN(x rstd) gamma).  The group's maximum is a 3-step
+// shuffle inside the eight lanes; a 1x32 block is the same half of four
+// lanes.
 // ---------------------------------------------------------------------------
-constexpr int kRmsChunks = 4;
+template <int kRec>
+__device__ __forceinline__ void quant_group8x16(float (&f)[2][8], bool ok, int sub, int64_t r, int64_t g,
+                                                int64_t M, int64_t atoms_k, uint8_t* codes, void* scales) {
+    uint2 c[2];
+    if (kRec == kRecMx) {
+        // halves h = 0, 1 lie in 1x32 blocks (sub / 4) and 2 + (sub / 4)
+        int e[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float a = amax8(f[h]);
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            e[h] = mx_exponent(a);
+            c[h] = encode8_mul(f[h], exp2_int(-e[h]));
+        }
+        const uint32_t b0 = (uint32_t)(e[0] + 127), b2 = (uint32_t)(e[1] + 127);
+        const int src = (threadIdx.x & 31) + 4;  // lane sub + 4: blocks 1 and 3 (used by sub = 0 only)
+        const uint32_t b1 = __shfl_sync(0xffffffffu, b0, src & 31);
+        const uint32_t b3 = __shfl_sync(0xffffffffu, b2, src & 31);
+        if (ok && sub == 0)
+            *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scales) + mx_scale_offset(r, 4 * g, atoms_k)) =
+                b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    } else {
+        float a = fmaxf(amax8(f[0]), amax8(f[1]));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+        if (kRec == kRecPow2) {
+            const int e = pow2_exponent(a);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) c[h] = encode8_mul(f[h], exp2_int(-e));
+            if (ok && sub == 0)
+                *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scales) + mx_scale_offset(r, 4 * g, atoms_k)) =
+                    (uint32_t)(e + 127) * 0x01010101u;
+        } else {
+            const float s = group_scale_bf16(a);
+            const Divider dv = make_divider(s);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) c[h] = encode8_div(f[h], dv);
+            if (ok && sub == 0) static_cast<float*>(scales)[g * M + r] = s;
+        }
+    }
+    if (ok) {
+        *reinterpret_cast<uint2*>(codes) = c[0];
+        *reinterpret_cast<uint2*>(codes + 64) = c[1];
+    }
+}
 
 template <int kRec, int kW>
 __global__ void __launch_bounds__(256, 4) k_rmsnorm_quant(const uint16_t* __restrict__ x,
@@ -138,20 +188,28 @@ __global__ void __launch_bounds__(256, 4) k_rmsnorm_quant(const uint16_t* __rest
     const int seg = warp % kW;
     const int64_t r = (int64_t)blockIdx.x * (8 / kW) + warp / kW;
     const bool row_ok = r < M;
-    const int64_t k0 = (int64_t)seg * 256 * kRmsChunks + 8 * lane;
+    const int gq = lane >> 3, sub = lane & 7;
     const uint16_t* xr = x + r * ld;
-    uint4 v[kRmsChunks];
+    // element of round j, half h: seg*1024 + j*512 + gq*128 + 64h + 8sub
+    const int64_t e0 = (int64_t)seg * 1024 + gq * 128 + 8 * sub;
+    uint4 v[2][2];
 #pragma unroll
-    for (int j = 0; j < kRmsChunks; ++j)
-        v[j] = (row_ok && k0 + 256 * j < K) ? ld_stream_v4(xr + k0 + 256 * j) : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t k = e0 + 512 * j + 64 * h;
+            v[j][h] = (row_ok && k < K) ? ld_stream_v4(xr + k) : make_uint4(0, 0, 0, 0);
+        }
     float ss = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kRmsChunks; ++j) {
-        float f[8];
-        unpack8(v[j], f);
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ss = __fmaf_rn(f[i], f[i], ss);
-    }
+        for (int h = 0; h < 2; ++h) {
+            float f[8];
+            unpack8(v[j][h], f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss = __fmaf_rn(f[i], f[i], ss);
+        }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
     if (kW > 1) {
@@ -166,25 +224,29 @@ __global__ void __launch_bounds__(256, 4) k_rmsnorm_quant(const uint16_t* __rest
     const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps));
     if (rstd_out != nullptr && seg == 0 && lane == 0) rstd_out[r] = rs;
     const int64_t atoms_k = (K + 127) / 128;
-    const int sub = lane & 15;
 #pragma unroll
-    for (int j = 0; j < kRmsChunks; ++j) {
-        const int64_t k = k0 + 256 * j;
-        if (k - 8 * lane >= K) break;                    // warp-uniform: the chunk is empty
-        const bool ok = k < K;                           // false only for the upper half of a half chunk
-        float f[8], gm[8];
-        unpack8(v[j], f);
-        unpack8(ok ? __ldg(reinterpret_cast<const uint4*>(gamma + k)) : make_uint4(0, 0, 0, 0), gm);
+    for (int j = 0; j < 2; ++j) {
+        const int64_t g0 = (int64_t)seg * 1024 + 512 * j;  // first element of the round
+        if (g0 >= K) break;                                // warp-uniform: the round is empty
+        const int64_t k = e0 + 512 * j;                     // this lane's first element
+        const bool ok = k < K;                              // K % 128 == 0: the lane's group is whole or absent
+        float f[2][8];
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-            const float2 t = mul2(mul2(make_float2(f[i], f[i + 1]), make_float2(rs, rs)),
-                                  make_float2(gm[i], gm[i + 1]));
-            f[i] = t.x;
-            f[i + 1] = t.y;
+        for (int h = 0; h < 2; ++h) {
+            float gm[8];
+            unpack8(v[j][h], f[h]);
+            unpack8(ok ? __ldg(reinterpret_cast<const uint4*>(gamma + k + 64 * h)) : make_uint4(0, 0, 0, 0), gm);
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                const float2 t = mul2(mul2(make_float2(f[h][i], f[h][i + 1]), make_float2(rs, rs)),
+                                      make_float2(gm[i], gm[i + 1]));
+                f[h][i] = t.x;
+                f[h][i + 1] = t.y;
+            }
+            const uint4 w = round8_bf16(f[h]);
+            if (y != nullptr && ok) *reinterpret_cast<uint4*>(y + r * ldy + k + 64 * h) = w;
         }
-        const uint4 w = round8_bf16(f);
-        if (y != nullptr && ok) *reinterpret_cast<uint4*>(y + r * ldy + k) = w;
-        quant_group16<kRec>(f, ok, sub, r, k / 128, M, atoms_k, codes + r * K + k, scales);
+        quant_group8x16<kRec>(f, ok, sub, r, k / 128, M, atoms_k, codes + r * K + k, scales);
     }
 }
 
@@ -283,7 +345,7 @@ template <int kRec>
 cudaError_t launch_rmsnorm_rec(const uint16_t* x, const uint16_t* gamma, int64_t M, int64_t K, int64_t ld, float eps,
                                uint16_t* y, int64_t ldy, float* rstd, uint8_t* codes, void* scales,
                                cudaStream_t st) {
-    const int64_t segs = (K + 256 * kRmsChunks - 1) / (256 * kRmsChunks);
+    const int64_t segs = (K + 1023) / 1024;
     const int w = segs <= 1 ? 1 : segs <= 2 ? 2 : segs <= 4 ? 4 : 8;
     const unsigned blocks = (unsigned)((M + (8 / w) - 1) / (8 / w));
 #define FP8BS_RMS(W) k_rmsnorm_quant<kRec, W><<<blocks, 256, 0, st>>>(x, gamma, M, K, ld, eps, y, ldy, rstd, codes, scales)
