@@ -8,8 +8,8 @@
 // tensor an unfused pipeline would hand to the quantizer), optionally writes
 // it, and quantizes those bf16 values in registers: 1x128 groups with fp32
 // scales, 1x128 groups with power-of-two scales, or MXFP8 1x32 blocks.  A
-// 128-element group is held by 16 lanes (8 values each), so its maximum is a
-// 4-step shuffle inside a half warp; a 1x32 block is 4 lanes.
+// 128-element group is held by 8 lanes (16 values each), so its maximum is a
+// 3-step shuffle; a 1x32 block is the same half of 4 lanes.
 #include "common.cuh"
 #include "kernels.h"
 #include "quant_common.cuh"
@@ -68,50 +68,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
     float y;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// Quantizes the 8 values of this lane, part of the 128-element group g of
-// row r held by the 16 lanes of a half warp (sub = lane % 16 holds elements
-// 8 sub .. 8 sub + 7 of the group).  All 32 lanes of the warp must call it
-// (the reductions are warp shuffles); a half warp with ok = false holds no
-// group and writes nothing.  Otherwise writes the lane's 8 codes at `codes`
-// and the group's scale(s).
-template <int kRec>
-__device__ __forceinline__ void quant_group16(const float (&y)[8], bool ok, int sub, int64_t r, int64_t g, int64_t M,
-                                              int64_t atoms_k, uint8_t* codes, void* scales) {
-    uint2 c;
-    if (kRec == kRecMx) {
-        float a = amax8(y);
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-        const int e = mx_exponent(a);
-        c = encode8_mul(y, exp2_int(-e));
-        // the four block exponents of the group (lanes sub = 0, 4, 8, 12)
-        const int base = threadIdx.x & 16;
-        const uint32_t b = (uint32_t)(e + 127);
-        const uint32_t b1 = __shfl_sync(0xffffffffu, b, base + 4, 32);
-        const uint32_t b2 = __shfl_sync(0xffffffffu, b, base + 8, 32);
-        const uint32_t b3 = __shfl_sync(0xffffffffu, b, base + 12, 32);
-        if (ok && sub == 0)
-            *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scales) + mx_scale_offset(r, 4 * g, atoms_k)) =
-                b | (b1 << 8) | (b2 << 16) | (b3 << 24);
-    } else {
-        float a = amax8(y);
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        if (kRec == kRecPow2) {
-            const int e = pow2_exponent(a);
-            c = encode8_mul(y, exp2_int(-e));
-            if (ok && sub == 0)
-                *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scales) + mx_scale_offset(r, 4 * g, atoms_k)) =
-                    (uint32_t)(e + 127) * 0x01010101u;
-        } else {
-            const float s = group_scale_bf16(a);
-            c = encode8_div(y, make_divider(s));
-            if (ok && sub == 0) static_cast<float*>(scales)[g * M + r] = s;
-        }
-    }
-    if (ok) *reinterpret_cast<uint2*>(codes) = c;
 }
 
 // ---------------------------------------------------------------------------
@@ -256,10 +212,11 @@ __global__ void __launch_bounds__(256, 4) k_rmsnorm_quant(const uint16_t* __rest
 // silu(g) = g sigmoid(g), sigmoid from e = exp(-|g|) as 1/(1+e) for g >= 0
 // and e/(1+e) for g < 0 (no overflow for large |g|); h is within one bf16
 // step of the exact value.  Work unit = one
-// 128-element group of one row (16 lanes); a 256-thread block takes 16 units
-// per round, 4 rounds with all loads issued first.
+// 128-element group of one row, eight lanes with 16 values each (elements
+// 8 sub .. and 64 + 8 sub .., as in the RMSNorm kernel); a 256-thread block
+// takes 32 units per round, 2 rounds with all loads issued first.
 // ---------------------------------------------------------------------------
-constexpr int kSwRounds = 4;
+constexpr int kSwRounds = 2;
 
 // silu(g) u for 8 pairs in fp32: sigmoid(g) = 1 / (1 + 2^(-g log2 e)) with
 // the hardware base-2 exponential and reciprocal approximations (relative
@@ -286,58 +243,64 @@ __global__ void __launch_bounds__(256, 4) k_swiglu_quant(const uint16_t* __restr
                                                       int64_t ld, uint16_t* __restrict__ h, int64_t ldh,
                                                       uint8_t* __restrict__ codes, void* __restrict__ scales) {
     const int64_t G = F / 128, units = M * G;
-    const int sub = threadIdx.x & 15;
+    const int sub = threadIdx.x & 7;
     const int64_t atoms_k = (F + 127) / 128;
-    const int64_t unit0 = (int64_t)blockIdx.x * kSwRounds * 16 + (threadIdx.x >> 4);
-    // (row, group) of each round's unit: one division, then steps of 16 units
+    const int64_t unit0 = (int64_t)blockIdx.x * kSwRounds * 32 + (threadIdx.x >> 3);
+    // (row, group) of each round's unit: one division, then steps of 32 units
     int64_t rr[kSwRounds], gg[kSwRounds];
     rr[0] = unit0 / G;
     gg[0] = unit0 - rr[0] * G;
 #pragma unroll
     for (int i = 1; i < kSwRounds; ++i) {
         rr[i] = rr[i - 1];
-        gg[i] = gg[i - 1] + 16;
+        gg[i] = gg[i - 1] + 32;
         while (gg[i] >= G) {
             gg[i] -= G;
             ++rr[i];
         }
     }
-    uint4 vg[kSwRounds], vu[kSwRounds];
+    uint4 vg[kSwRounds][2], vu[kSwRounds][2];
 #pragma unroll
-    for (int i = 0; i < kSwRounds; ++i) {
-        if (unit0 + 16 * i < units) {
-            const uint16_t* p = gu + rr[i] * ld + gg[i] * 128 + 8 * sub;
-            vg[i] = ld_stream_v4(p);
-            vu[i] = ld_stream_v4(p + F);
-        } else {
-            vg[i] = vu[i] = make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < kSwRounds; ++i)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            if (unit0 + 32 * i < units) {
+                const uint16_t* p = gu + rr[i] * ld + gg[i] * 128 + 64 * hh + 8 * sub;
+                vg[i][hh] = ld_stream_v4(p);
+                vu[i][hh] = ld_stream_v4(p + F);
+            } else {
+                vg[i][hh] = vu[i][hh] = make_uint4(0, 0, 0, 0);
+            }
         }
-    }
 #pragma unroll
     for (int i = 0; i < kSwRounds; ++i) {
-        if (unit0 - (threadIdx.x >> 4) + 16 * i >= units) break;   // block-uniform
-        const bool ok = unit0 + 16 * i < units;
+        if (unit0 - (threadIdx.x >> 3) + 32 * i >= units) break;   // block-uniform
+        const bool ok = unit0 + 32 * i < units;
         const int64_t r = ok ? rr[i] : 0, g = ok ? gg[i] : 0, k = g * 128 + 8 * sub;
-        float fg[8], fu[8];
-        unpack8(vg[i], fg);
-        unpack8(vu[i], fu);
-        const float gmin = fminf(fminf(fminf(fg[0], fg[1]), fminf(fg[2], fg[3])),
-                                 fminf(fminf(fg[4], fg[5]), fminf(fg[6], fg[7])));
-        float gsave[8];
+        float fg[2][8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) gsave[q] = fg[q];
-        silu_times8(fg, fu);
-        if (gmin < -80.0f) {
+        for (int hh = 0; hh < 2; ++hh) {
+            float fu[8];
+            unpack8(vg[i][hh], fg[hh]);
+            unpack8(vu[i][hh], fu);
+            const float gmin = fminf(fminf(fminf(fg[hh][0], fg[hh][1]), fminf(fg[hh][2], fg[hh][3])),
+                                     fminf(fminf(fg[hh][4], fg[hh][5]), fminf(fg[hh][6], fg[hh][7])));
+            float gsave[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (gsave[q] < -80.0f) {
-                    const float e = expf(gsave[q]);
-                    fg[q] = __fmul_rn(__fmul_rn(gsave[q], __fdiv_rn(e, __fadd_rn(1.0f, e))), fu[q]);
-                }
+            for (int q = 0; q < 8; ++q) gsave[q] = fg[hh][q];
+            silu_times8(fg[hh], fu);
+            if (gmin < -80.0f) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (gsave[q] < -80.0f) {
+                        const float e = expf(gsave[q]);
+                        fg[hh][q] = __fmul_rn(__fmul_rn(gsave[q], __fdiv_rn(e, __fadd_rn(1.0f, e))), fu[q]);
+                    }
+            }
+            const uint4 w = round8_bf16(fg[hh]);
+            if (h != nullptr && ok) *reinterpret_cast<uint4*>(h + r * ldh + k + 64 * hh) = w;
         }
-        const uint4 w = round8_bf16(fg);
-        if (h != nullptr && ok) *reinterpret_cast<uint4*>(h + r * ldh + k) = w;
-        quant_group16<kRec>(fg, ok, sub, r, g, M, atoms_k, codes + r * F + k, scales);
+        quant_group8x16<kRec>(fg, ok, sub, r, g, M, atoms_k, codes + r * F + k, scales);
     }
 }
 
@@ -380,7 +343,7 @@ cudaError_t launch_swiglu_quant(const uint16_t* gu, int64_t M, int64_t F, int64_
         if (e != cudaSuccess) return e;
     }
     const int64_t units = M * (F / 128);
-    const unsigned blocks = (unsigned)((units + 16 * kSwRounds - 1) / (16 * kSwRounds));
+    const unsigned blocks = (unsigned)((units + 32 * kSwRounds - 1) / (32 * kSwRounds));
     if (recipe == kRecPow2)
         k_swiglu_quant<kRecPow2><<<blocks, 256, 0, st>>>(gu, M, F, ld, h, ldh, codes, scales);
     else if (recipe == kRecMx)
