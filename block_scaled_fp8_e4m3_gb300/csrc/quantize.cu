@@ -332,18 +332,24 @@ __device__ __forceinline__ void store_tile_transposed(const uint8_t* tile, int t
 // 128x128 blocks.  Block = one weight block; thread (chunk = t%16, rg = t/16)
 // holds rows 8rg..8rg+7 of columns 8chunk..8chunk+7 (eight 16-byte loads in
 // flight).  The block maximum is a warp shuffle reduction followed by a
-// shared-memory reduction over the 8 warps.  The optional transposed copy
-// goes through a shared-memory tile (row stride 144 B) read column-wise; each
-// thread writes 32 contiguous transposed bytes (one full sector).
+// shared-memory reduction over the 8 warps.  The optional transposed copy:
+// each thread transposes its four 4x4 byte blocks of codes in registers
+// (byte permutes), which gives for each of its 8 columns the words of rows
+// 8rg..8rg+3 and 8rg+4..8rg+7, and stores them into a shared tile of 128
+// transposed rows x 32 words whose 16-byte units are permuted by
+// (row / 8) % 8; each thread then writes 64 contiguous bytes of one
+// transposed row.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ int blk_t_word(int c, int wi) {
+    return c * 32 + ((((wi >> 2) ^ (c >> 3)) & 7) << 2) + (wi & 3);
+}
 template <bool kPow2>
 __global__ void __launch_bounds__(256) k_quant_block(const uint16_t* __restrict__ w, int64_t N, int64_t K,
                                                      int64_t ld, uint8_t* __restrict__ codes,
                                                      void* __restrict__ scales, uint8_t* __restrict__ codes_t,
                                                      void* __restrict__ scales_t) {
-    constexpr int kStride = 144;
     __shared__ float red[8];
-    __shared__ __align__(16) uint8_t tile[128 * kStride];
+    __shared__ __align__(16) uint32_t tile_t[128 * 32];
 
     const int64_t KB = K / 128, NB = N / 128;
     const int64_t nb = (int64_t)blockIdx.x / KB, kb = (int64_t)blockIdx.x % KB;
@@ -388,17 +394,36 @@ __global__ void __launch_bounds__(256) k_quant_block(const uint16_t* __restrict_
         }
         dv = make_divider(s);
     }
+    uint2 c[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         float f[8];
         unpack8(v[i], f);
-        const uint2 c = kPow2 ? encode8_mul(f, mul) : encode8_div(f, dv);
-        *reinterpret_cast<uint2*>(codes + (n0 + rg * 8 + i) * K + k0 + chunk * 8) = c;
-        if (codes_t) *reinterpret_cast<uint2*>(tile + (rg * 8 + i) * kStride + chunk * 8) = c;
+        c[i] = kPow2 ? encode8_mul(f, mul) : encode8_div(f, dv);
+        *reinterpret_cast<uint2*>(codes + (n0 + rg * 8 + i) * K + k0 + chunk * 8) = c[i];
     }
     if (codes_t == nullptr) return;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            // rows 8rg + 4k .. +3 x columns 8chunk + 4hh .. +3: word i = row i, byte j = column j
+            const uint32_t w0 = hh ? c[4 * k].y : c[4 * k].x, w1 = hh ? c[4 * k + 1].y : c[4 * k + 1].x;
+            const uint32_t w2 = hh ? c[4 * k + 2].y : c[4 * k + 2].x, w3 = hh ? c[4 * k + 3].y : c[4 * k + 3].x;
+            const uint32_t t0 = __byte_perm(w0, w1, 0x5140), t1 = __byte_perm(w2, w3, 0x5140);
+            const uint32_t t2 = __byte_perm(w0, w1, 0x7362), t3 = __byte_perm(w2, w3, 0x7362);
+            const uint32_t col[4] = {__byte_perm(t0, t1, 0x5410), __byte_perm(t0, t1, 0x7632),
+                                     __byte_perm(t2, t3, 0x5410), __byte_perm(t2, t3, 0x7632)};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tile_t[blk_t_word(chunk * 8 + hh * 4 + j, 2 * rg + k)] = col[j];
+        }
     __syncthreads();
-    store_tile_transposed<kStride>(tile, t, codes_t + k0 * N + n0, N);
+    // transposed row cr (column cr of the block), 16-byte units 4q .. 4q + 3
+    const int cr = t >> 1, q = t & 1;
+    const uint4* row = reinterpret_cast<const uint4*>(tile_t) + cr * 8;
+    uint4* dst = reinterpret_cast<uint4*>(codes_t + (k0 + cr) * N + n0 + 64 * q);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) dst[u] = row[((4 * q + u) ^ (cr >> 3)) & 7];
 }
 
 // ---------------------------------------------------------------------------
