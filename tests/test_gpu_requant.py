@@ -103,3 +103,29 @@ def test_random_row_scales_full_significands():
     ct, st = oracle.requant_1x128_to_128x1_T(codes, srow)
     assert_bytes_equal(to_np(qt.codes), ct, "codes^T")
     assert_bytes_equal(to_np(qt.scales), st, "scales")
+
+
+def test_nan_codes_in_the_saved_activation():
+    """E4M3 NaN codes (0x7F, 0xFF) in the saved activation: as documented
+    for fp8_requantize_transposed, each gives a NaN code (either sign) at its
+    transposed position and stays out of its group's scale; every other code
+    and every scale equals the oracle's."""
+    x = synth.random_bf16((256, 256), seed=91, outliers=True)
+    q = fp8.quantize_group(x.to(DEV), "K")
+    codes = to_np(q.codes).copy()
+    rng = np.random.default_rng(92)
+    pos = rng.choice(codes.size, size=40, replace=False)
+    codes.flat[pos[:20]] = 0x7F
+    codes.flat[pos[20:]] = 0xFF
+    srow = to_np(q.scales)
+    qn = fp8.QTensor(torch.from_numpy(codes).to(DEV), torch.from_numpy(srow).to(DEV), 256, 256, fp8.RECIPE_BLOCKWISE,
+                     fp8.LAYOUT_GROUP_1x128)
+    qt = fp8.requantize_transposed(qn)
+    ct, st = oracle.requant_1x128_to_128x1_T(codes, srow)
+    got = to_np(qt.codes)
+    nan_g, nan_r = (got & 0x7F) == 0x7F, (ct & 0x7F) == 0x7F
+    assert np.array_equal(nan_g, nan_r)
+    assert nan_g.sum() == 40
+    assert_bytes_equal(np.where(nan_g, 0x7F, got).astype(np.uint8), np.where(nan_r, 0x7F, ct).astype(np.uint8),
+                       "codes^T outside the NaN positions")
+    assert_bytes_equal(to_np(qt.scales), st, "scales")
