@@ -125,10 +125,20 @@ __device__ __forceinline__ void promote16_cols(uint64_t* acc2, const uint32_t* r
     }
 }
 
-// Cluster c of C visits the 256x256 tiles c, c + C, ...
-__device__ __forceinline__ void bw_tile(int t, int tiles_n, int& tm, int& tn) {
-    tm = t / tiles_n;
-    tn = t - tm * tiles_n;
+// Cluster c of C visits the 256x256 tiles c, c + C, ...  Tile t is numbered
+// down bands of 16 tile rows (the last band may be shorter): within a band the
+// index walks down the rows first, then across the columns.  The clusters
+// running at one time then share the A rows of one band and a few B column
+// tiles, which stay in L2, instead of each column tile of B being fetched
+// again for every row of tiles.
+__device__ __forceinline__ void bw_tile(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
+    constexpr int kBand = 16;
+    const int band = t / (kBand * tiles_n);
+    const int first = band * kBand;
+    const int rows = tiles_m - first < kBand ? tiles_m - first : kBand;
+    const int idx = t - band * kBand * tiles_n;
+    tm = first + idx % rows;
+    tn = idx / rows;
 }
 
 template <uint32_t R>
@@ -195,7 +205,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
                 const uint32_t full_leader = mapa_shared(&bar->full[0], 0);  // + 8 * stage
                 int tm = 0, tn = 0, kb = 0, ti = 0;
                 for (int g = 0; g < total; ++g) {
-                    if (kb == 0) bw_tile(cid + ti * ncl, p.tiles_n, tm, tn);
+                    if (kb == 0) bw_tile(cid + ti * ncl, p.tiles_m, p.tiles_n, tm, tn);
                     const int s = g % kBwStages;
                     if (!mbar_wait_bounded(&bar->empty[s], ((g / kBwStages) & 1) ^ 1, abort, p.st, 1)) break;
                     uint8_t* stage = smem + s * kBwStageBytes;
@@ -241,7 +251,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
             const int nblocks = p.N / 128;
             int tm = 0, tn = 0, kb = 0, ti = 0;
             for (int g = 0; g < total; ++g) {
-                if (kb == 0) bw_tile(cid + ti * ncl, p.tiles_n, tm, tn);
+                if (kb == 0) bw_tile(cid + ti * ncl, p.tiles_m, p.tiles_n, tm, tn);
                 const int slot = g % kBwScaleSlots;
                 if (!mbar_wait_bounded(&bws->sc_empty[slot], ((g / kBwScaleSlots) & 1) ^ 1, abort, p.st, 7)) break;
 #pragma unroll
@@ -298,7 +308,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         bool ok = true;
         for (int ti = 0; ti < my_tiles && ok; ++ti) {
             int ctm, ctn;
-            bw_tile(cid + ti * ncl, p.tiles_n, ctm, ctn);
+            bw_tile(cid + ti * ncl, p.tiles_m, p.tiles_n, ctm, ctn);
             uint64_t acc2[kBwCols / 2];
 #pragma unroll
             for (int i = 0; i < kBwCols / 2; ++i) acc2[i] = 0ull;

@@ -108,13 +108,22 @@ struct TileCoord {
     int tn;
 };
 
-// Cluster tile -> (group, 256-row cluster tile, 256-column tile) by binary
-// search over the prefix of cluster tiles per group; then this CTA's half.
-__device__ __forceinline__ TileCoord mx_tile(int tile, int tiles_n, const int* pfx, const int* pfx2, const int* offs,
+// Cluster tile -> (group, 256-row cluster tile, 256-column tile); then this
+// CTA's half.  Cluster tiles are numbered down bands of 16 cluster-tile rows
+// (the last band may be shorter), rows first within a band, so that the pairs
+// running at one time share a band of A and a few column tiles of B in L2;
+// the group comes from a binary search over the prefix of cluster tiles per
+// group.
+__device__ __forceinline__ TileCoord mx_tile(int tile, int tiles_m, int tiles_n, const int* pfx, const int* pfx2, const int* offs,
                                             int G, uint32_t rank) {
     TileCoord c;
-    const int mt2_global = tile / tiles_n;
-    c.tn = tile - mt2_global * tiles_n;
+    constexpr int kBand = 16;
+    const int band = tile / (kBand * tiles_n);
+    const int first = band * kBand;
+    const int rows = tiles_m - first < kBand ? tiles_m - first : kBand;
+    const int idx = tile - band * kBand * tiles_n;
+    const int mt2_global = first + idx % rows;
+    c.tn = idx / rows;
     int lo = 0, hi = G;  // largest g with pfx2[g] <= mt2_global
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -232,7 +241,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             const int atoms_k = p.K / 128;
             const int b_atom_rows = (p.G * p.N + 127) / 128;
             for (int tile = cid; tile < num_tiles && ok; tile += ncl) {
-                const TileCoord c = mx_tile(tile, p.tiles_n, pfx, pfx2, offs, G, rank);
+                const TileCoord c = mx_tile(tile, bar->num_mtiles, p.tiles_n, pfx, pfx2, offs, G, rank);
                 const int bcol0 = c.g * p.N + c.tn * kMxBN;        // first B row of the tile
                 const int batom0 = bcol0 / 128;                      // its scale atom row
                 const int batom1 = c.tn * kMxBN + 128 < p.N && batom0 + 1 < b_atom_rows ? batom0 + 1 : batom0;
@@ -336,7 +345,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const int64_t q_atoms_k = (p.N + 127) / 128;
         uint32_t aph = 0;
         for (int tile = cid; tile < num_tiles; tile += ncl) {
-            const TileCoord c = mx_tile(tile, p.tiles_n, pfx, pfx2, offs, G, rank);
+            const TileCoord c = mx_tile(tile, bar->num_mtiles, p.tiles_n, pfx, pfx2, offs, G, rank);
             const int rl = 32 * q + lane;
             const int ncol0 = c.tn * kMxBN + 128 * h;
             const bool mvalid = rl < c.rows, hvalid = ncol0 < p.N;
