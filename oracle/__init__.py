@@ -59,7 +59,7 @@ def load():
         "oracle_gemm_ref": (None, [_P, _P, _I64, _I64, _I64, _P, _P]),
         "oracle_gemm_ref_sampled": (None, [_P, _P, _I64, _P, _P, _I64, _P, _P]),
         "oracle_naive_requant_per_tensor": (C.c_float, [_P, _P, _I64, _I64, _P]),
-        "oracle_splitmix64": (C.c_uint64, [C.c_uint64]),
+        "oracle_sync_word_term": (C.c_uint64, [C.c_uint64, C.c_uint64]),
         "oracle_sync_checksum": (C.c_uint64, [_P, C.c_uint64]),
         "oracle_sync_payload_size": (C.c_uint64, [_P, C.c_int32]),
         "oracle_sync_pack": (C.c_uint64, [_P, C.c_int32, _P, C.c_uint64]),
@@ -368,8 +368,9 @@ def naive_requant_per_tensor(codes, block_scales):
     return out, float(s)
 
 
-def splitmix64(x: int) -> int:
-    return int(load().oracle_splitmix64(x & 0xFFFFFFFFFFFFFFFF))
+def sync_word_term(w: int, i: int) -> int:
+    """The checksum's term for payload word w at word index i."""
+    return int(load().oracle_sync_word_term(w & 0xFFFFFFFFFFFFFFFF, i & 0xFFFFFFFFFFFFFFFF))
 
 
 class _Entry(C.Structure):

@@ -814,7 +814,7 @@ float oracle_naive_requant_per_tensor(const uint8_t* codes, const float* block_s
 /*                                                                            */
 /* The byte format is this library's own definition (the pages give none):    */
 /*   header, 64 bytes, little-endian:                                         */
-/*     0 u64 magic "FP8SYNC1"   8 u32 version (1)   12 u32 n_entries          */
+/*     0 u64 magic "FP8SYNC1"   8 u32 version (2)   12 u32 n_entries          */
 /*    16 u64 total_bytes       24 u64 data_offset   32 u64 checksum           */
 /*    40..63 zero                                                             */
 /*   entry table at 64, 128 bytes per entry:                                  */
@@ -825,9 +825,18 @@ float oracle_naive_requant_per_tensor(const uint8_t* codes, const float* block_s
 /*   segments: data (codes or bf16 values) then scales, each starting at a    */
 /*   256-byte boundary, zero padded; total_bytes is a multiple of 256;        */
 /*   data_offset = roundup(64 + 128 n, 256).                                  */
-/*   checksum: sum over the 8-byte words w_i at byte offsets 8i >= 64 of      */
-/*   splitmix64(w_i XOR i), mod 2^64 (splitmix64 finaliser of Steele, Lea and */
-/*   Flood, "Fast splittable pseudorandom number generators", 2014).          */
+/*   checksum: for each 8-byte word w_i at byte offset 8i >= 64, with lo_i   */
+/*   and hi_i its low and high 32-bit halves,                                 */
+/*     t_i = ((lo_i + i K1) mod 2^32) * ((hi_i + i K2) mod 2^32),             */
+/*   K1 = 0x9E3779B9, K2 = 0x85EBCA6B, and checksum = sum of t_i mod 2^64:    */
+/*   the NH inner product of UMAC (Black, Halevi, Krawczyk, Krovetz and       */
+/*   Rogaway, "UMAC: Fast and Secure Message Authentication", CRYPTO 1999)    */
+/*   with keys taken from the word index.  A change to one half of one word   */
+/*   changes t_i by delta * (the other factor), |delta|, factor < 2^32, so it */
+/*   is always detected unless that word's other factor is 0 mod 2^32; the    */
+/*   keys repeat every 2^32 words (32 GiB).  (Version 1 of the format summed  */
+/*   the splitmix64 finaliser of w_i XOR i instead: about eight times the     */
+/*   integer work per word.)                                                  */
 /* parity unpinned (format): pinned only by round-trip and corruption tests.  */
 /* ------------------------------------------------------------------------ */
 
@@ -841,15 +850,15 @@ typedef struct {
     const uint8_t* scales;
 } oracle_sync_entry;
 
-static uint64_t mix64(uint64_t z)
+/* t_i of the checksum for word w at word index i */
+static uint64_t nh_term(uint64_t w, uint64_t i)
 {
-    z += 0x9E3779B97F4A7C15ULL;
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
-    return z ^ (z >> 31);
+    const uint32_t a = (uint32_t)(w & 0xFFFFFFFFu) + (uint32_t)(i & 0xFFFFFFFFu) * 0x9E3779B9u;
+    const uint32_t b = (uint32_t)(w >> 32) + (uint32_t)(i & 0xFFFFFFFFu) * 0x85EBCA6Bu;
+    return (uint64_t)a * (uint64_t)b;
 }
 
-uint64_t oracle_splitmix64(uint64_t x) { return mix64(x); }
+uint64_t oracle_sync_word_term(uint64_t w, uint64_t i) { return nh_term(w, i); }
 
 static uint64_t rd64(const uint8_t* p)
 {
@@ -898,7 +907,7 @@ uint64_t oracle_sync_checksum(const uint8_t* payload, uint64_t total_bytes)
 {
     uint64_t sum = 0;
     for (uint64_t i = 8; i < total_bytes / 8; ++i)
-        sum += mix64(rd64(payload + 8 * i) ^ i);
+        sum += nh_term(rd64(payload + 8 * i), i);
     return sum;
 }
 
@@ -944,7 +953,7 @@ uint64_t oracle_sync_pack(const oracle_sync_entry* e, int32_t n, uint8_t* payloa
     }
     memset(payload, 0, (size_t)total);
     wr64(payload + 0, SYNC_MAGIC);
-    wr32(payload + 8, 1);
+    wr32(payload + 8, 2);
     wr32(payload + 12, (uint32_t)n);
     wr64(payload + 16, total);
     wr64(payload + 24, round_up(64 + 128 * (uint64_t)n, 256));
@@ -980,7 +989,7 @@ int32_t oracle_sync_install(const uint8_t* payload, uint64_t bytes,
                             const oracle_sync_entry* dst, int32_t n)
 {
     if (bytes < 64) return 1;
-    if (rd64(payload) != SYNC_MAGIC || rd32(payload + 8) != 1 ||
+    if (rd64(payload) != SYNC_MAGIC || rd32(payload + 8) != 2 ||
         rd32(payload + 12) != (uint32_t)n)
         return 1;
     uint64_t total = rd64(payload + 16);

@@ -58,7 +58,7 @@ def test_layout(orc):
     specs = _specs(orc)
     p = orc.sync_pack(specs)
     assert bytes(p[:8]) == b"FP8SYNC1"
-    assert _rd(p, 8, 4) == 1 and _rd(p, 12, 4) == len(specs)
+    assert _rd(p, 8, 4) == 2 and _rd(p, 12, 4) == len(specs)
     total = _rd(p, 16, 8)
     assert total == p.size and total % 256 == 0
     assert _rd(p, 24, 8) == 768                       # roundup(64 + 4*128, 256)
@@ -82,13 +82,61 @@ def test_layout(orc):
     assert _rd(p, 40, 24) == 0
 
 
-def test_splitmix64_published_outputs(orc):
-    """The finaliser used by the checksum reproduces the published first
-    outputs of the splitmix64 generator started from state 0."""
-    rows = read_golden("splitmix64.txt")
-    gamma = 0x9E3779B97F4A7C15
-    for i, row in enumerate(rows):
-        assert orc.splitmix64((gamma * i) & (2 ** 64 - 1)) == int(row[1], 16)
+def test_checksum_is_the_sum_of_word_terms(orc):
+    """The checksum field equals the sum mod 2^64 of the per-word terms over
+    the words at byte offsets >= 64 (the header's own words excluded), with
+    the checksum field itself counted as zero when the sum was formed."""
+    specs = _specs(orc)
+    p = orc.sync_pack(specs)
+    q = p.copy()
+    q[32:40] = 0
+    words = q.view("<u8")
+    total = sum(orc.sync_word_term(int(w), i) for i, w in enumerate(words) if i >= 8) % 2 ** 64
+    assert total == _rd(p, 32, 8) == orc.sync_checksum(p)
+
+
+def test_word_term_is_bilinear_in_the_keyed_halves(orc):
+    """t(w, i) = ((lo + i K1) mod 2^32) ((hi + i K2) mod 2^32): with the key
+    sums a, b of a word, adding d to lo (no wrap of a) changes t by exactly
+    d * b, adding d to hi changes it by d * a, and t is the product a * b --
+    checked against keys recovered from words whose halves are zero, so a
+    swapped pair of halves, a wrong key or a dropped key fails."""
+    rng = np.random.default_rng(11)
+    K1, K2 = 0x9E3779B9, 0x85EBCA6B
+    for _ in range(200):
+        i = int(rng.integers(8, 2 ** 40))
+        ka = (i * K1) % 2 ** 32                         # key sums of the zero word
+        kb = (i * K2) % 2 ** 32
+        assert orc.sync_word_term(0, i) == ka * kb
+        lo, hi = int(rng.integers(0, 2 ** 32)), int(rng.integers(0, 2 ** 32))
+        a, b = (lo + ka) % 2 ** 32, (hi + kb) % 2 ** 32
+        w = lo | (hi << 32)
+        t = orc.sync_word_term(w, i)
+        assert t == a * b
+        d = int(rng.integers(1, 2 ** 16))
+        if a + d < 2 ** 32 and (lo + d) < 2 ** 32:
+            assert orc.sync_word_term(w + d, i) == t + d * b
+        if b + d < 2 ** 32 and (hi + d) < 2 ** 32:
+            assert orc.sync_word_term(w + (d << 32), i) == t + d * a
+    # keys depend on the index modulo 2^32 words only
+    assert orc.sync_word_term(12345, 7) == orc.sync_word_term(12345, 7 + 2 ** 32)
+
+
+def test_checksum_detects_every_single_bit_flip(orc):
+    """Flipping any one of the 64 bits of a word changes its term by
+    +-2^b times the other keyed half, which is nonzero whenever that half is
+    (true for every word of this payload), so every single-bit flip of the
+    covered region is detected: all 64 bits of 40 words spread over the
+    header tail, the table, data, padding and scales."""
+    specs = _specs(orc)
+    p = orc.sync_pack(specs)
+    base = orc.sync_checksum(p)
+    nwords = p.size // 8
+    for wi in np.linspace(8, nwords - 1, 40).astype(int):
+        for bit in range(64):
+            q = p.copy()
+            q[8 * wi + bit // 8] ^= 1 << (bit % 8)
+            assert orc.sync_checksum(q) != base, (wi, bit)
 
 
 def test_checksum_detects_any_single_word_change(orc):
