@@ -143,15 +143,17 @@ int64_t mx_scale_bytes(int64_t rows, int64_t cols) { return cdiv(rows, 128) * cd
 
 // ---------------------------------------------------------------- sync layout
 constexpr uint64_t kSyncMagic = 0x31434E5953385046ull;  // bytes "FP8SYNC1"
+constexpr uint32_t kSyncVersion = 2;                     // the NH checksum
 constexpr uint64_t kHeaderBytes = 64, kEntryBytes = 128;
 
 uint64_t round_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
 
-uint64_t host_mix64(uint64_t z) {
-    z += 0x9E3779B97F4A7C15ull;
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-    return z ^ (z >> 31);
+// The checksum term of payload word w at word index i (format version 2):
+// ((lo + i K1) mod 2^32) * ((hi + i K2) mod 2^32), summed mod 2^64.
+uint64_t word_term(uint64_t w, uint64_t i) {
+    const uint32_t a = (uint32_t)w + (uint32_t)i * 0x9E3779B9u;
+    const uint32_t b = (uint32_t)(w >> 32) + (uint32_t)i * 0x85EBCA6Bu;
+    return (uint64_t)a * b;
 }
 
 struct EntryLayout {
@@ -231,7 +233,7 @@ std::vector<uint8_t> build_table(const fp8_sync_entry* e, int32_t n, const std::
     const uint64_t data_offset = round_up(kHeaderBytes + kEntryBytes * (uint64_t)n, 256);
     std::vector<uint8_t> h((size_t)data_offset, 0);
     put64(&h[0], kSyncMagic);
-    put32(&h[8], 1);
+    put32(&h[8], kSyncVersion);
     put32(&h[12], (uint32_t)n);
     put64(&h[16], total);
     put64(&h[24], data_offset);
@@ -253,7 +255,7 @@ std::vector<uint8_t> build_table(const fp8_sync_entry* e, int32_t n, const std::
 
 uint64_t table_checksum(const std::vector<uint8_t>& h) {
     uint64_t sum = 0;
-    for (uint64_t i = kHeaderBytes / 8; i < h.size() / 8; ++i) sum += host_mix64(get64(&h[(size_t)(8 * i)]) ^ i);
+    for (uint64_t i = kHeaderBytes / 8; i < h.size() / 8; ++i) sum += word_term(get64(&h[(size_t)(8 * i)]), i);
     return sum;
 }
 
@@ -340,7 +342,7 @@ void fill_table(uint8_t* h, uint64_t data_offset, const fp8_sync_entry* e, int32
                 uint64_t total) {
     memset(h, 0, (size_t)data_offset);
     put64(&h[0], kSyncMagic);
-    put32(&h[8], 1);
+    put32(&h[8], kSyncVersion);
     put32(&h[12], (uint32_t)n);
     put64(&h[16], total);
     put64(&h[24], data_offset);
@@ -860,8 +862,8 @@ fp8_status fp8_sync_install(const void* payload_dev, uint64_t bytes, const fp8_s
         e = cudaMemcpyAsync(got.data(), pay, got.size(), cudaMemcpyDeviceToHost, cs);
         if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
         if (e != cudaSuccess) return cuda_fail(e, "sync_install header read");
-        if (get64(&got[0]) != kSyncMagic || get32(&got[8]) != 1)
-            return fail(FP8_ERR_BAD_PAYLOAD, "not a version-1 FP8 sync payload");
+        if (get64(&got[0]) != kSyncMagic || get32(&got[8]) != kSyncVersion)
+            return fail(FP8_ERR_BAD_PAYLOAD, "not a version-2 FP8 sync payload");
         if (get32(&got[12]) != (uint32_t)n)
             return fail(FP8_ERR_BAD_PAYLOAD, "payload has %u entries, %d destinations", get32(&got[12]), n);
         for (size_t i = 0; i < expect.size(); ++i) {
@@ -958,8 +960,8 @@ fp8_status fp8_sync_install_noalloc(const void* payload_dev, uint64_t bytes, con
     cudaError_t e = cudaMemcpyAsync(got, pay, (size_t)data_offset, cudaMemcpyDeviceToHost, cs);
     if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
     if (e != cudaSuccess) return cuda_fail(e, "sync_install_noalloc header read");
-    if (get64(&got[0]) != kSyncMagic || get32(&got[8]) != 1)
-        return fail(FP8_ERR_BAD_PAYLOAD, "not a version-1 FP8 sync payload");
+    if (get64(&got[0]) != kSyncMagic || get32(&got[8]) != kSyncVersion)
+        return fail(FP8_ERR_BAD_PAYLOAD, "not a version-2 FP8 sync payload");
     if (get32(&got[12]) != (uint32_t)n)
         return fail(FP8_ERR_BAD_PAYLOAD, "payload has %u entries, %d destinations", get32(&got[12]), n);
     for (uint64_t i = 0; i < data_offset; ++i) {
@@ -969,7 +971,7 @@ fp8_status fp8_sync_install_noalloc(const void* payload_dev, uint64_t bytes, con
     }
     put64(&got[32], 0);
     unsigned long long table_sum = 0;
-    for (uint64_t i = kHeaderBytes / 8; i < data_offset / 8; ++i) table_sum += host_mix64(get64(&got[8 * i]) ^ i);
+    for (uint64_t i = kHeaderBytes / 8; i < data_offset / 8; ++i) table_sum += word_term(get64(&got[8 * i]), i);
 
     fp8_status se;
     NoAllocScratch* sc = noalloc_scratch(&se);

@@ -10,9 +10,12 @@
 //    stored in its header by the last block to finish;
 //  - scatter: batched copy out of the payload, skipped entirely when the
 //    verification failed.
-// Checksum = sum of splitmix64(w_i XOR i) over 8-byte words w_i at byte
-// offsets 8i >= 64, mod 2^64 (the splitmix64 finaliser of Steele, Lea and
-// Flood, 2014).  Being a sum, it can be accumulated in any order.
+// Checksum (payload format version 2): over the 8-byte words w_i at byte
+// offsets 8i >= 64, with lo_i, hi_i their 32-bit halves, the sum mod 2^64 of
+//   ((lo_i + i * 0x9E3779B9) mod 2^32) * ((hi_i + i * 0x85EBCA6B) mod 2^32),
+// the NH inner product of UMAC (Black, Halevi, Krawczyk, Krovetz, Rogaway,
+// CRYPTO 1999) keyed by the word index: one 32x32->64 multiply-add per word.
+// Being a sum, it can be accumulated in any order.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -20,11 +23,14 @@ namespace fp8bs {
 
 namespace {
 
-__device__ __forceinline__ unsigned long long mix64(unsigned long long z) {
-    z += 0x9E3779B97F4A7C15ull;
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-    return z ^ (z >> 31);
+// The checksum terms of one 16-byte chunk: words (v.x, v.y) at word index
+// i0 and (v.z, v.w) at i0 + 1 (keys need the index modulo 2^32 only).
+__device__ __forceinline__ unsigned long long chunk_terms(const uint4& v, uint64_t i0) {
+    constexpr uint32_t kK1 = 0x9E3779B9u, kK2 = 0x85EBCA6Bu;
+    const uint32_t i = (uint32_t)i0;
+    const uint32_t a0 = v.x + i * kK1, b0 = v.y + i * kK2;
+    const uint32_t a1 = v.z + (i + 1u) * kK1, b1 = v.w + (i + 1u) * kK2;
+    return (unsigned long long)a0 * b0 + (unsigned long long)a1 * b1;
 }
 
 struct SegTable {
@@ -116,10 +122,7 @@ __global__ void __launch_bounds__(256) k_sync_pack(const SegTable tab, unsigned 
                 const CopySeg& sg = tab.seg[sidx[u]];
                 const uint64_t off = (cc - start[sidx[u]]) * 16;
                 *reinterpret_cast<uint4*>(sg.dst + off) = v[u];
-                const unsigned long long w0 = (unsigned long long)v[u].x | ((unsigned long long)v[u].y << 32);
-                const unsigned long long w1 = (unsigned long long)v[u].z | ((unsigned long long)v[u].w << 32);
-                const unsigned long long i0 = sg.dst_word0 + off / 8;
-                sum += mix64(w0 ^ i0) + mix64(w1 ^ (i0 + 1));
+                sum += chunk_terms(v[u], sg.dst_word0 + off / 8);
             }
         }
     }
@@ -145,11 +148,7 @@ __device__ __forceinline__ unsigned long long verify_part(const uint8_t* __restr
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     const uint4* p4 = reinterpret_cast<const uint4*>(payload);
     unsigned long long sum = 0;
-    auto mix_chunk = [&](const uint4& v, uint64_t cc) {
-        const unsigned long long w0 = (unsigned long long)v.x | ((unsigned long long)v.y << 32);
-        const unsigned long long w1 = (unsigned long long)v.z | ((unsigned long long)v.w << 32);
-        sum += mix64(w0 ^ (2 * cc)) + mix64(w1 ^ (2 * cc + 1));
-    };
+    auto mix_chunk = [&](const uint4& v, uint64_t cc) { sum += chunk_terms(v, 2 * cc); };
     // whole rounds of kUnroll chunks: one bounds check per round, and the
     // next round's loads issued before this round is mixed
     uint64_t c = c0 + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -179,20 +178,60 @@ __device__ __forceinline__ unsigned long long verify_part(const uint8_t* __restr
     return block_sum(sum);
 }
 
-// Thread 0 of the block that finishes last: the verdict from the complete
-// sum, then the accumulator is reset for the next call.
-__device__ __forceinline__ void finish_verdict(const uint8_t* payload, unsigned long long table_sum, StatusBlock* st) {
-    __threadfence();
-    const unsigned long long total = atomicAdd(&st->sum, 0ull) + table_sum;
-    const unsigned long long stored = *reinterpret_cast<const unsigned long long*>(payload + 32);
-    const unsigned int header_bad = atomicExch(&st->header_bad, 0u);
+// ---- arrival at the end of the checksum pass (thread 0 of each block)
+__device__ __forceinline__ unsigned int atom_add_acq_rel_gpu(unsigned int* p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned int ld_relaxed_gpu(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Adds the block's partial sum (a reduction that does not wait for its
+// result) and counts the block in with one acq_rel increment, which orders
+// the sum before it; true in the block that arrives last, which then sees
+// every block's sum and the header/table flag of block 0.
+__device__ __forceinline__ bool arrive_last(StatusBlock* st, unsigned long long bs) {
+    if (bs != 0) atomicAdd(&st->sum, bs);
+    return atom_add_acq_rel_gpu(&st->blocks_done, 1u) == gridDim.x - 1;
+}
+
+// In the last block: the verdict (1 when the sum or the header/table check
+// fails), written to the status block.  `stored` is the payload's checksum
+// field, read when the block started.
+__device__ __forceinline__ unsigned int decide_verdict(StatusBlock* st, unsigned long long table_sum,
+                                                       unsigned long long stored, unsigned int& header_bad) {
+    const unsigned long long total = ld_relaxed_gpu(&st->sum) + table_sum;
+    header_bad = ld_relaxed_gpu(&st->header_bad);
     const unsigned int bad = (total != stored || header_bad) ? 1u : 0u;
     st->verdict = bad;
+    return bad;
+}
+
+// After the verdict is out: error bits, and the accumulators reset for the
+// next call (which runs after this kernel in stream order).
+__device__ __forceinline__ void close_verdict(StatusBlock* st, unsigned int bad, unsigned int header_bad) {
     if (header_bad) atomicOr(&st->error_bits, kErrBadPayload);
     else if (bad) atomicOr(&st->error_bits, kErrChecksum);
     st->sum = 0;
+    st->header_bad = 0;
     st->blocks_done = 0;
-    __threadfence();
 }
 
 // This block's share of the segment copies payload -> destinations.
@@ -240,11 +279,13 @@ __device__ __forceinline__ void scatter_part(const SegTable& tab) {
 __global__ void __launch_bounds__(256) k_sync_verify(const uint8_t* __restrict__ payload, uint64_t data_offset,
                                                      uint64_t total_bytes, unsigned long long table_sum,
                                                      StatusBlock* st, const __grid_constant__ ExpectTable expect) {
+    unsigned long long stored = 0;
+    if (threadIdx.x == 0) stored = *reinterpret_cast<const unsigned long long*>(payload + 32);
     const unsigned long long bs = verify_part(payload, data_offset, total_bytes, st, expect);
-    if (threadIdx.x == 0) {
-        atomicAdd(&st->sum, bs);
-        __threadfence();
-        if (atomicAdd(&st->blocks_done, 1u) == gridDim.x - 1) finish_verdict(payload, table_sum, st);
+    if (threadIdx.x == 0 && arrive_last(st, bs)) {
+        unsigned int header_bad;
+        const unsigned int bad = decide_verdict(st, table_sum, stored, header_bad);
+        close_verdict(st, bad, header_bad);
     }
 }
 
@@ -257,36 +298,45 @@ __global__ void __launch_bounds__(256) k_sync_scatter(const SegTable tab, const 
 // blocks checksum the payload, meet at a grid barrier kept in the status
 // block, and copy only if the verdict is clean -- no destination byte is
 // written before the whole payload has been verified.  The second read of
-// the payload mostly hits L2.  The barrier wait is bounded: on expiry the
-// block records a timeout (site 40) and copies nothing.
+// the payload mostly hits L2.  The block that arrives last decides and
+// releases the others with one store of the barrier generation, which
+// carries the verdict (+2 clean, +3 mismatch), so the barrier costs the
+// arrival increment, one load of the sum and that store.  The wait is
+// bounded: on expiry the block records a timeout (site 40) and copies
+// nothing.
 __global__ void __launch_bounds__(256) k_sync_install(const uint8_t* __restrict__ payload, uint64_t data_offset,
                                                       uint64_t total_bytes, unsigned long long table_sum,
                                                       StatusBlock* st, const __grid_constant__ ExpectTable expect,
                                                       const __grid_constant__ SegTable tab) {
     __shared__ unsigned int proceed;
     unsigned int gen0 = 0;
-    if (threadIdx.x == 0) gen0 = *reinterpret_cast<volatile unsigned int*>(&st->barrier_gen);
+    unsigned long long stored = 0;
+    if (threadIdx.x == 0) {
+        gen0 = ld_relaxed_gpu(&st->barrier_gen);
+        stored = *reinterpret_cast<const unsigned long long*>(payload + 32);
+    }
     const unsigned long long bs = verify_part(payload, data_offset, total_bytes, st, expect);
     if (threadIdx.x == 0) {
-        atomicAdd(&st->sum, bs);
-        __threadfence();
-        unsigned int go = 1;
-        if (atomicAdd(&st->blocks_done, 1u) == gridDim.x - 1) {
-            finish_verdict(payload, table_sum, st);
-            atomicExch(&st->barrier_gen, gen0 + 1u);
+        unsigned int go;
+        if (arrive_last(st, bs)) {
+            unsigned int header_bad;
+            const unsigned int bad = decide_verdict(st, table_sum, stored, header_bad);
+            st_release_gpu(&st->barrier_gen, gen0 + 2u + bad);
+            close_verdict(st, bad, header_bad);
+            go = bad ? 0u : 1u;
         } else {
             const unsigned long long t0 = global_timer_ns();
-            while (*reinterpret_cast<volatile unsigned int*>(&st->barrier_gen) == gen0) {
+            unsigned int g;
+            while ((g = ld_acquire_gpu(&st->barrier_gen)) == gen0) {
                 if (global_timer_ns() - t0 > kWaitLimitNs) {
                     report_timeout(st, 40);
-                    go = 0;
                     break;
                 }
                 __nanosleep(64);
             }
-            __threadfence();
+            go = g == gen0 + 2u ? 1u : 0u;
         }
-        proceed = go && *reinterpret_cast<volatile unsigned int*>(&st->verdict) == 0;
+        proceed = go;
     }
     __syncthreads();
     if (proceed) scatter_part(tab);

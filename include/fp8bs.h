@@ -357,7 +357,7 @@ fp8_status fp8_grouped_gemm(const fp8_tensor* A, const fp8_tensor* B_stack,
 /* rather than being inferred by each side).                               */
 /*                                                                         */
 /* Payload bytes (little-endian):                                          */
-/*   header 64 B: u64 magic "FP8SYNC1", u32 version 1, u32 n_entries,      */
+/*   header 64 B: u64 magic "FP8SYNC1", u32 version 2, u32 n_entries,      */
 /*     u64 total_bytes, u64 data_offset, u64 checksum, 24 zero bytes;      */
 /*   n entries of 128 B at byte 64: u64 tag, u32 kind, u32 recipe,         */
 /*     i64 rows, i64 cols, u32 layout, u32 0, u64 data_offset,             */
@@ -365,8 +365,12 @@ fp8_status fp8_grouped_gemm(const fp8_tensor* A, const fp8_tensor* B_stack,
 /*   segments from data_offset = roundup(64 + 128 n, 256): each entry's    */
 /*     data then scales, each 256-byte aligned, zero padded; total_bytes   */
 /*     is a multiple of 256.                                               */
-/*   checksum = sum over 8-byte words w_i at offsets 8i >= 64 of           */
-/*     splitmix64(w_i XOR i) mod 2^64.                                     */
+/*   checksum = sum over 8-byte words w_i at offsets 8i >= 64, lo_i and    */
+/*     hi_i their 32-bit halves, of ((lo_i + i 0x9E3779B9) mod 2^32) *     */
+/*     ((hi_i + i 0x85EBCA6B) mod 2^32), mod 2^64 (the NH inner product of */
+/*     UMAC, Black et al., CRYPTO 1999, keyed by the word index).  Any     */
+/*     change to one 32-bit half of one word is detected unless the        */
+/*     word's other keyed half is 0 mod 2^32.                              */
 /* ---------------------------------------------------------------------- */
 
 /* Payload size for these entries (host-only computation). */
