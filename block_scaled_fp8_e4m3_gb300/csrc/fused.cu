@@ -20,9 +20,11 @@ namespace {
 
 enum : int { kRecFp32 = 0, kRecPow2 = 1, kRecMx = 2 };
 
+// Two fp32 values rounded to bf16 (nearest, ties to even), lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+    uint32_t w;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
+    return w;
 }
 
 // Rounds 8 fp32 results to bf16: returns the packed words and, in f, the
@@ -56,6 +58,35 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     float2 r;
     asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
     return r;
+}
+
+// A bf16 pair (low element in the low half) as an fp32 pair in one 64-bit
+// register, ready for the packed fp32x2 instructions.
+__device__ __forceinline__ uint64_t bf16x2_f32x2(uint32_t w) {
+    uint64_t r;
+    asm("{\n\t.reg .b32 lo, hi;\n\tshl.b32 lo, %1, 16;\n\tand.b32 hi, %1, 0xFFFF0000;\n\tmov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(r)
+        : "r"(w));
+    return r;
+}
+
+// An fp32 pair rounded to a bf16 pair (nearest, ties to even).
+__device__ __forceinline__ uint32_t f32x2_bf16x2(uint64_t p) {
+    uint32_t w;
+    asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.bf16x2.f32 %0, hi, lo;\n\t}" : "=r"(w) : "l"(p));
+    return w;
+}
+
+__device__ __forceinline__ uint64_t fma2_rn(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t mul2_rn(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -156,16 +187,25 @@ __global__ void __launch_bounds__(256, 4) k_rmsnorm_quant(const uint16_t* __rest
             const int64_t k = e0 + 512 * j + 64 * h;
             v[j][h] = (row_ok && k < K) ? ld_stream_v4(xr + k) : make_uint4(0, 0, 0, 0);
         }
-    float ss = 0.0f;
+    // sum of squares: even and odd elements in the two halves of a packed pair
+    uint64_t ss2 = 0ull;
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            float f[8];
-            unpack8(v[j][h], f);
+            const uint32_t wd[4] = {v[j][h].x, v[j][h].y, v[j][h].z, v[j][h].w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ss = __fmaf_rn(f[i], f[i], ss);
+            for (int q = 0; q < 4; ++q) {
+                const uint64_t p = bf16x2_f32x2(wd[q]);
+                ss2 = fma2_rn(p, p, ss2);
+            }
         }
+    float ss;
+    {
+        float lo, hi;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(ss2));
+        ss = __fadd_rn(lo, hi);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
     if (kW > 1) {
@@ -187,20 +227,22 @@ __global__ void __launch_bounds__(256, 4) k_rmsnorm_quant(const uint16_t* __rest
         const int64_t k = e0 + 512 * j;                     // this lane's first element
         const bool ok = k < K;                              // K % 128 == 0: the lane's group is whole or absent
         float f[2][8];
+        uint64_t rs2;
+        asm("mov.b64 %0, {%1, %1};" : "=l"(rs2) : "f"(rs));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            float gm[8];
-            unpack8(v[j][h], f[h]);
-            unpack8(ok ? __ldg(reinterpret_cast<const uint4*>(gamma + k + 64 * h)) : make_uint4(0, 0, 0, 0), gm);
+            const uint4 gv = ok ? __ldg(reinterpret_cast<const uint4*>(gamma + k + 64 * h)) : make_uint4(0, 0, 0, 0);
+            const uint32_t xw[4] = {v[j][h].x, v[j][h].y, v[j][h].z, v[j][h].w};
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            uint32_t yw[4];
 #pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-                const float2 t = mul2(mul2(make_float2(f[h][i], f[h][i + 1]), make_float2(rs, rs)),
-                                      make_float2(gm[i], gm[i + 1]));
-                f[h][i] = t.x;
-                f[h][i + 1] = t.y;
+            for (int q = 0; q < 4; ++q) {
+                // y = RN_bf16(RN(x rstd) gamma), two elements per instruction
+                yw[q] = f32x2_bf16x2(mul2_rn(mul2_rn(bf16x2_f32x2(xw[q]), rs2), bf16x2_f32x2(gw[q])));
+                f[h][2 * q] = bf16_lo(yw[q]);
+                f[h][2 * q + 1] = bf16_hi(yw[q]);
             }
-            const uint4 w = round8_bf16(f[h]);
-            if (y != nullptr && ok) *reinterpret_cast<uint4*>(y + r * ldy + k + 64 * h) = w;
+            if (y != nullptr && ok) *reinterpret_cast<uint4*>(y + r * ldy + k + 64 * h) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
         }
         quant_group8x16<kRec>(f, ok, sub, r, k / 128, M, atoms_k, codes + r * K + k, scales);
     }
