@@ -14,7 +14,8 @@
 //    a 128-wide K block is four MMAs (one thread issues a tcgen05 instruction
 //    every ~60 cycles; N=128 halves would double that and starve the pipe);
 //  * each CTA stages its 128 rows of A and its half (128 rows) of the tile's
-//    B rows: 32 KB per SM per K block, six-stage TMA ring;
+//    B rows: 32 KB per SM per K block, four-stage TMA ring (measured faster
+//    than six, five or three stages);
 //  * two 256-column TMEM sets hold the partials of consecutive K blocks;
 //    two threads issue the MMAs (even and odd K blocks), so the thread that
 //    may reuse a set is never the one blocked issuing the other set;
@@ -32,7 +33,7 @@ namespace fp8bs {
 namespace {
 
 constexpr int kBwBN = 256;                                 // tile columns (both CTAs)
-constexpr int kBwStages = 6;                               // one 128-wide K block per stage
+constexpr int kBwStages = 4;                               // one 128-wide K block per stage
 constexpr uint32_t kBwABytes = 128 * BK;                   // 16 KB: this CTA's 128 rows of A
 constexpr uint32_t kBwBBytes = 128 * BK;                   // 16 KB: this CTA's 128 rows of B
 constexpr uint32_t kBwStageBytes = kBwABytes + kBwBBytes;  // 32 KB
