@@ -114,6 +114,22 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 tensor map over a row-major [rows][ld] matrix of which the first
+// cols columns are addressed, for stores of 64-column (128-byte) x 128-row
+// boxes from a 128-byte-swizzled shared tile; rows and columns outside the
+// matrix are not written.  base 16-byte aligned, ld * 2 a multiple of 16.
+bool make_map_store_bf16(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows, uint64_t ld) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D u8 tensor map, no swizzle, over a row-major [rows][cols] byte array.
 bool make_map_plain_u8(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
     auto fn = encode_fn();
